@@ -1,0 +1,434 @@
+#!/usr/bin/env python3
+"""Benchmark of the CSA2 layer on GB300: one JSON line on rank 0.
+
+A step is one pass of the decoder-tail block under SWA bounded replay over the
+8 x 8192-token extend workload (8 requests, tail 128 rows each = 1024 query
+rows): the tail layout, the L20-style source pass over the tail rows
+(full-visible FP4 scoring, top-512 + candidate pool, attention with the normal
+window), the L21-style Reindex layer (scoring restricted to the pool, top-512,
+attention with the tail window) and the L22-style Reuse layer (attention with
+L21's indices).  value = layer-queries per second = 3 layers x 1024 rows x
+ranks / step time.  Inputs are resident in HBM; L2 is flushed between timed
+steps.  `e2e` times the same step through the same calls with the inputs
+copied from pinned host memory and the outputs copied back every step.
+
+--impl reference times the CPU oracle (the baseline arm of this build) on a
+bounded sample of the same workload.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA2 layer queries/s at 1 GB300; achieved HBM GB/s and % roofline"
+UNIT = "layer-queries/s"
+ROW_BYTES = 512 + 16 * 4          # one FP8 block-32 row: codes + fp32 scales
+LAYERS = ("L20", "L21", "L22")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thr = threading.Thread(target=self._read, daemon=True)
+            self.thr.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def max_over_ranks(ms, device, world):
+    """Slowest rank's step time (the whole job finishes when the last rank does)."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def layer_queries_per_s(rows, world, ms):
+    """Whole-job throughput: every rank's rows through every layer of the step."""
+    return len(LAYERS) * rows * world / (ms * 1e-3)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured"
+    return 6800.0, 1700.0, "fallback"
+
+
+def attn_algorithmic_bytes(w, runner, layer, win_lo):
+    """Bytes the method itself reads and writes in one attention launch: per
+    query the selected rows plus its window rows (576 B each), Q and O (bf16),
+    the index row (int32) and the lse (fp32)."""
+    import torch
+    nq = runner.nq
+    pos = runner.batches[layer]["q_pos"].to(torch.int64)
+    lo = pos - w.window + 1
+    if win_lo is not None:
+        lo = torch.maximum(lo, win_lo)
+    lo = torch.clamp(lo, min=0)
+    n_win = int((pos - lo + 1).clamp(min=0).sum())
+    if layer == "L22":      # Reuse: the Reindex layer's indices
+        n_sel = int((runner.idx["L21"] >= 0).sum())
+    else:
+        n_sel = int(runner.count[layer].sum())
+    per_q = w.n_heads * 512 * 2 * 2 + w.topk * 4 + w.n_heads * 4
+    return (n_sel + n_win) * ROW_BYTES + nq * per_q
+
+
+def bench_ours(args, rank, world, local_rank):
+    import torch
+    import sparse_attention_prefill_gb300 as S
+    from sparse_attention_prefill_gb300 import synth
+    from sparse_attention_prefill_gb300.layer import LayerRunner
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    S.load()
+    w = synth.config("c2_decoder_replay", dev, args.seed + rank)
+    run = LayerRunner(w)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)    # > 129 MB L2
+    launches_per_step = 9   # tail 1; L20 score 1 + candidates 2 + attn 1; L21 3; L22 1
+
+    # attention launches are bracketed by events on the launching stream
+    attn_ev = []
+
+    def step(record=False):
+        run.decoder_tail_step(attn_ev if record else None)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    times = []
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t_wall = time.perf_counter()
+    for _ in range(args.steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step(record=True)
+        e1.record(stream)
+        times.append((e0, e1))
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in times]
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), dev, world)
+    assert int(run.d_err.item()) == 0, "device data-error flags raised during the bench"
+    rows = run.nq
+    value = layer_queries_per_s(rows, world, ms)
+
+    # dominant kernel: the attention launches
+    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+    byts = [attn_algorithmic_bytes(w, run, "L20", None),
+            attn_algorithmic_bytes(w, run, "L21", run.tail_win_lo),
+            attn_algorithmic_bytes(w, run, "L22", run.tail_win_lo)]
+    per_launch_bytes = sum(byts) / 3
+    hbm, bf16_sus, peak_kind = measured_peaks()
+    achieved = per_launch_bytes / (attn_avg_ms * 1e-3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "attn_traffic.json")
+    if os.path.exists(tpath):
+        tj = json.load(open(tpath))
+        if tj.get("kernel_id") == run_kernel_id():
+            traffic = tj.get("traffic_bytes_per_launch")
+    roofline = {"bound": "hbm", "kernel": "csa2_sparse_swa_attn", "achieved": round(achieved, 1),
+                "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "traffic": traffic, "peak_source": peak_kind,
+                "algorithmic_bytes_per_launch": int(per_launch_bytes),
+                "avg_launch_ms": round(attn_avg_ms, 4),
+                "share_of_step": round(sum(attn_ms) / sum(step_ms), 3)}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = bench_e2e(args, w, run, dev, rank, world)
+
+    return dict(value=value, ms=ms, wall=wall, clocks=clk, roofline=roofline, e2e=e2e,
+                launches=launches_per_step * args.steps, rows=rows, w=w)
+
+
+def run_kernel_id():
+    """Identity of the attention kernel build (source hash) so that stored ncu
+    traffic is only reported for the kernel it was measured on."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("attn_tc.cu", "attn_simt.cu"):
+        p = os.path.join(ROOT, "sparse_attention_prefill_gb300", "csrc", f)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def bench_e2e(args, w, run, dev, rank, world):
+    """Same step through the same calls, inputs from pinned host memory and the
+    step's outputs read back, copies inside the timed region."""
+    import torch
+    host_in, dev_in = [], []
+
+    def reg(t):
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        host_in.append(h)
+        dev_in.append(t)
+
+    p = w.pool
+    for t in (p.kv_fp8, p.kv_scale, p.k_fp4, p.k_scale, p.kv_start, p.kv_len, w.extend_len,
+              w.seq_len):
+        reg(t)
+    for L in w.layers.values():
+        for t in (L.q, L.swa_fp8, L.swa_scale, L.swa_start, L.swa_pos0, L.swa_len, L.q_fp4,
+                  L.q_scale, L.head_w):
+            if t is not None:
+                reg(t)
+    outs = [run.out[n] for n in LAYERS] + [run.lse[n] for n in LAYERS] + [run.idx["L21"]]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        run.decoder_tail_step()
+        for h, d in zip(host_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ts) / len(ts), dev, world)
+    return {"value": layer_queries_per_s(run.nq, world, ms), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(ms, 4)}
+
+
+def oracle_sample_step(w, rows_per_req, threads):
+    """One bounded sample of the step on the CPU oracle: the same three layers
+    for `rows_per_req` tail rows of every request."""
+    import numpy as np
+    import torch
+    from oracle import api as O
+
+    O.set_threads(threads)
+    npy = lambda t: None if t is None else (t.cpu().view(torch.int16).numpy().view(np.uint16)
+                                            if t.dtype == torch.bfloat16 else t.cpu().numpy())
+    tail, _ = O.tail_layout(npy(w.extend_len), npy(w.seq_len), w.window)
+    sel = np.concatenate([np.arange(tail["cu_tail"][r + 1] - rows_per_req, tail["cu_tail"][r + 1])
+                          for r in range(w.num_req)])
+    rows = torch.from_numpy(sel)
+    base = {k: npy(v) if torch.is_tensor(v) else v for k, v in w.batch("L20").items()}
+    base["q_req"], base["q_pos"], base["num_q"] = tail["row_req"][sel], tail["pos"][sel], len(sel)
+    win = tail["win_lo"][sel]
+    L = w.layers
+    lt = lambda n, a: npy(getattr(L[n], a)[rows]) if getattr(L[n], a) is not None else None
+    kf, ks, kv, kvs = npy(w.pool.k_fp4), npy(w.pool.k_scale), npy(w.pool.kv_fp8), npy(w.pool.kv_scale)
+    b20 = dict(base, swa_start=npy(L["L20"].swa_start), swa_pos0=npy(L["L20"].swa_pos0),
+               swa_len=npy(L["L20"].swa_len))
+    s, _ = O.index_score(b20, lt("L20", "q_fp4"), lt("L20", "q_scale"), lt("L20", "head_w"), kf,
+                         ks, w.ld)
+    i20, _, blk, _, _ = O.topk_candidates(b20, np.nan_to_num(s, nan=-np.inf), w.topk, w.block,
+                                          w.max_blocks)
+    O.sparse_swa_attn(b20, lt("L20", "q"), kv, kvs, i20, npy(L["L20"].swa_fp8),
+                      npy(L["L20"].swa_scale), None, w.window, w.sm_scale)
+    b21 = dict(base, swa_start=npy(L["L21"].swa_start), swa_pos0=npy(L["L21"].swa_pos0),
+               swa_len=npy(L["L21"].swa_len))
+    s21, _ = O.index_score(b21, lt("L21", "q_fp4"), lt("L21", "q_scale"), lt("L21", "head_w"),
+                           kf, ks, w.max_blocks * w.block, cand_blocks=blk, block=w.block)
+    i21, _, _ = O.topk(b21, np.nan_to_num(s21, nan=-np.inf), w.topk, cand_blocks=blk,
+                       block=w.block)
+    O.sparse_swa_attn(b21, lt("L21", "q"), kv, kvs, i21, npy(L["L21"].swa_fp8),
+                      npy(L["L21"].swa_scale), win, w.window, w.sm_scale)
+    b22 = dict(base, swa_start=npy(L["L22"].swa_start), swa_pos0=npy(L["L22"].swa_pos0),
+               swa_len=npy(L["L22"].swa_len))
+    O.sparse_swa_attn(b22, lt("L22", "q"), kv, kvs, i21, npy(L["L22"].swa_fp8),
+                      npy(L["L22"].swa_scale), win, w.window, w.sm_scale)
+    return len(sel)
+
+
+def cpu_threads():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def cpu_baseline(w, budget_s=15.0):
+    """The oracle, as it stands, on a bounded sample of the workload."""
+    threads = cpu_threads()
+    rows_per_req = 2
+    t0 = time.perf_counter()
+    n = oracle_sample_step(w, rows_per_req, threads)
+    dt = time.perf_counter() - t0
+    reps = 1
+    while time.perf_counter() - t0 < budget_s * 0.5 and reps < 4:
+        n += oracle_sample_step(w, rows_per_req, threads)
+        reps += 1
+    dt = time.perf_counter() - t0
+    return {"value": len(LAYERS) * n / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "%d x (%d tail rows per request x 8 requests) through the 3-layer step"
+                      % (reps, rows_per_req)}
+
+
+def config_block(w, extra=None):
+    d = {"workload": "c2_decoder_replay: decoder tail block under SWA bounded replay, "
+                     "8 requests x 8192-token extend (m=1, 8192 FP8 block-32 KV rows + "
+                     "MXFP4 index keys per request), tail 128 rows/request at pos 8064-8191; "
+                     "layers L20-style source (full scoring, top-512, <=2048x8 pool), "
+                     "L21-style Reindex in pool, L22-style Reuse; 64 q heads x 512, "
+                     "32 index heads x 128; top-512; SWA window 128",
+         "query_rows": w.num_q, "layers_per_step": len(LAYERS), "requests": w.num_req,
+         "l2": "flushed between timed steps (256 MB write)", "seed": 0}
+    if extra:
+        d.update(extra)
+    return d
+
+
+def main():
+    args = parse()
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        import torch
+        from sparse_attention_prefill_gb300 import synth
+        from oracle import build as ob
+        ob.build_oracle()
+        w = synth.config("c2_decoder_replay", "cpu", args.seed)
+        threads = cpu_threads()
+        for _ in range(args.warmup):
+            oracle_sample_step(w, 1, threads)
+        ts = []
+        n = 0
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            n += oracle_sample_step(w, 1, threads)
+            ts.append(time.perf_counter() - t0)
+        ms = 1e3 * sum(ts) / len(ts)
+        value = len(LAYERS) * n / sum(ts)
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": config_block(w, {"sample": "1 tail row per request (8 rows) per step"}),
+                "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                 "sample": "1 tail row per request x 8 requests per step"},
+                "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    from oracle import build as ob
+    if rank == 0 and not args.no_cpu:
+        ob.build_oracle()
+    r = bench_ours(args, rank, world, local_rank)
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu:
+            from sparse_attention_prefill_gb300 import synth
+            cpu = cpu_baseline(synth.config("c2_decoder_replay", "cpu", args.seed))
+        line = {"metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32", "data": "synthetic",
+                "config": config_block(r["w"], {"parallelism": "replicas" if world > 1 else "1gpu"}),
+                "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r["e2e"],
+                "clocks": r["clocks"], "gpu_launches": r["launches"],
+                "wall_s_timed_region": round(r["wall"], 4)}
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,240 @@
+/*
+ * csa2.h -- C ABI of libcsa2.so: the CSA2 attention layer (DeepSeek-V4.1) as it
+ * runs under decoder-side SWA bounded replay, on one GB300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is DEVICE memory allocated and owned by the caller,
+ *    except `const csa2_batch *b`, which is a host struct holding device
+ *    pointers, and is read during the call only.  The library allocates
+ *    nothing and keeps no state between calls; results are written only to the
+ *    output arrays named below.
+ *  - Work is enqueued on `stream` (0 = legacy default stream); no entry point
+ *    synchronises the host.  Calls are thread-safe.
+ *  - Return value: CSA2_OK, or a status describing an argument the host could
+ *    check before launching (nothing is launched then), or CSA2_ERR_CUDA if a
+ *    launch failed.
+ *  - Data errors the host cannot see (an index out of range, a window without
+ *    stored rows, ...) never fault: the kernel skips the offending element,
+ *    keeps the rest of the result well defined, and ORs a CSA2_DERR_* bit into
+ *    `*d_err` (an int32 in device memory; pass NULL to ignore).  d_err is never
+ *    cleared by the library.
+ *
+ * Storage formats
+ *  - MXFP4 (index queries and keys): E2M1 codes, two per byte, element 2i in
+ *    the low nibble and 2i+1 in the high nibble; one fp32 scale per 32
+ *    consecutive elements.  Scales must be powers of two in [2^-23, 2^12]
+ *    (the MX scale is an E8M0 power of two); others set CSA2_DERR_SCALE and
+ *    are rounded to the nearest power of two.
+ *  - FP8 block-32 rows (compressed KV and SWA): 512 E4M3 (OCP "FN") codes per
+ *    row plus 16 fp32 scales, one per 32 channels; value = e4m3 * scale.  The
+ *    dequantised values must lie inside the f16 range (|x| < 65504).
+ *  - Queries are bf16 and must lie inside the f16 range; outputs are bf16.
+ *
+ * Citations name the page and section that define each operation:
+ *  [TAIL] "SGLang 如何让 DeepSeek V4.1 Flash 的后半层只处理尾部 token"
+ *         (lab.ttaoai.cn notes on decoder SWA bounded replay), sec. 2.1-2.6.
+ *  [CSA2] "DeepSeek V4.1 Flash 建模" (pages.haorui.li), CSA2 card and the
+ *         Hierarchical Sparse Indexer card; mixed-precision card for formats.
+ *  [D0]   SGLang/Miles day-0 article (theainews.cc), sec. 1, 2, 4.2 and 5.
+ */
+#ifndef CSA2_H_
+#define CSA2_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *csa2_stream_t; /* same object as cudaStream_t */
+
+#if defined(__GNUC__)
+#define CSA2_API __attribute__((visibility("default")))
+#else
+#define CSA2_API
+#endif
+
+/* status codes */
+#define CSA2_OK 0
+#define CSA2_ERR_INVALID_ARG 1 /* host-checked argument error; nothing launched */
+#define CSA2_ERR_UNSUPPORTED 2 /* valid request this build does not implement */
+#define CSA2_ERR_CUDA 3        /* a kernel launch failed */
+#define CSA2_ERR_TIMEOUT 4     /* reserved */
+
+/* data-error bits ORed into *d_err */
+#define CSA2_DERR_RANGE_IDX 1     /* a selected index outside [0, n_vis) or past kv_len */
+#define CSA2_DERR_RANGE_WINDOW 2  /* a window position without a stored SWA row */
+#define CSA2_DERR_RANGE_CTX 4     /* n_vis(t) exceeds the request's stored entries */
+#define CSA2_DERR_SCALE 8         /* an MXFP4 scale that is not an in-range power of two */
+#define CSA2_DERR_LD 16           /* a score row longer than the row stride `ld` */
+#define CSA2_DERR_CAPACITY 32     /* tail rows beyond the output capacity */
+#define CSA2_DERR_BAD_EXTEND 64   /* an extend with E < 0 or S < E */
+
+/* Rows of one layer call.  Host struct; every array is device memory.
+ *   q_req[Nq]   request of each query row (0 <= q_req < num_req)
+ *   q_pos[Nq]   ABSOLUTE token position t of each query row
+ *   kv_start[R] pool row holding the request's compressed entry 0, in both the
+ *               compressed-KV pool and the index-key pool (entry j of request
+ *               r is pool row kv_start[r] + j)
+ *   kv_len[R]   compressed entries stored for the request
+ *   swa_start[R], swa_pos0[R], swa_len[R]: the layer's SWA rows of request r
+ *               hold absolute positions swa_pos0[r] .. swa_pos0[r]+swa_len[r]-1
+ *               at rows swa_start[r] .. swa_start[r]+swa_len[r]-1
+ *   ratio       m in {1, 2}: each compressed entry covers m consecutive tokens
+ *               without overlap, so entry j is visible to position t once its
+ *               last token m*j+m-1 <= t: n_vis(t) = floor((t+1)/m)
+ *               ([CSA2] "压缩器也改了"; [D0] sec. 1). */
+typedef struct csa2_batch {
+  int32_t num_q;
+  int32_t num_req;
+  int32_t ratio;
+  int32_t reserved;
+  const int32_t *q_req;
+  const int64_t *q_pos;
+  const int64_t *kv_start;
+  const int64_t *kv_len;
+  const int64_t *swa_start;
+  const int64_t *swa_pos0;
+  const int64_t *swa_len;
+} csa2_batch;
+
+/* Human-readable name of a status code (static storage). */
+CSA2_API const char *csa2_status_string(int status);
+
+/* ---------------------------------------------------------------------------
+ * a1. Decoder bounded-replay tail layout   [TAIL] sec. 2.1, 2.2, 2.5, 2.6 and
+ * the formula box: T = min(window, E); kept positions [S-T, S); lower bound S-T.
+ *
+ * For each request r with extend length E_r = extend_len[r] and sequence length
+ * S_r = seq_len[r] after the extend, the late layers keep the last
+ * T_r = min(window, E_r) rows of this extend, per request (never one cut of
+ * the whole batch):
+ *   tail_len[r]  = T_r                                         [R]
+ *   cu_tail[r]   = T_0 + ... + T_{r-1}, cu_tail[R] = total     [R+1]
+ *   for k < T_r, row i = cu_tail[r] + k:
+ *     src_row[i] = cu_E[r] + E_r - T_r + k   (row in the packed extend, cu_E
+ *                                             = exclusive prefix sum of E)
+ *     pos[i]     = S_r - T_r + k             (absolute; never renumbered)
+ *     win_lo[i]  = S_r - T_r                 (absolute window lower bound)
+ *     row_req[i] = r                         (optional; may be NULL)
+ * Rows at or beyond `capacity` are not written (CSA2_DERR_CAPACITY); a
+ * capacity of window*num_req always suffices.  E_r < 0 or S_r < E_r gives
+ * T_r = 0 and CSA2_DERR_BAD_EXTEND.  num_req >= 0; window >= 1.
+ * ------------------------------------------------------------------------- */
+CSA2_API int csa2_tail_layout(int32_t num_req, const int32_t *extend_len,
+                     const int64_t *seq_len, int32_t window, int32_t *tail_len,
+                     int32_t *cu_tail, int32_t *src_row, int64_t *pos,
+                     int64_t *win_lo, int32_t *row_req, int64_t capacity,
+                     int32_t *d_err, csa2_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * a2-a4, a7. Index scores   [CSA2] CSA2 and Hierarchical cards; [D0] sec. 2
+ * and sec. 5 ("FP4 索引与 TP 布局": MQA-shaped, heads replicated).
+ *
+ *   s(q, j) = sum_h w[q,h] * max(0, sum_d Qi[q,h,d] * Ki[j,d])
+ *
+ * q_fp4   [Nq, n_heads, head_dim/2] MXFP4 codes;  q_scale [Nq, n_heads, head_dim/32]
+ * head_w  [Nq, n_heads] fp32, or NULL for all ones
+ * k_fp4   [Nk, head_dim/2];  k_scale [Nk, head_dim/32]: the index-key pool
+ *         (entry j of request r at row kv_start[r] + j)
+ * cand_blocks == NULL (Full / Reindex over all visible entries): row q of
+ *         `scores` receives columns j = 0 .. n_vis(t)-1.
+ * cand_blocks != NULL (Reindex restricted to the candidate pool): [Nq,
+ *         max_blocks] ascending block ids, -1 padded; row q receives slots
+ *         s = 0 .. nb*block-1 (nb = leading non-negative ids), slot s scoring
+ *         entry cand_blocks[q, s/block]*block + s%block, or -inf when that
+ *         entry is not visible.
+ * scores  [Nq, ld] fp32, row stride ld; columns past each row's length are not
+ *         written.  A row longer than ld is cut at ld (CSA2_DERR_LD); n_vis
+ *         past kv_len is cut at kv_len (CSA2_DERR_RANGE_CTX).
+ * Supported: head_dim == 128, n_heads in {8, 16, 32, 64}, block in [1, 64],
+ * max_blocks in [1, 4096].
+ * ------------------------------------------------------------------------- */
+CSA2_API int csa2_index_score(const csa2_batch *b, int32_t n_heads, int32_t head_dim,
+                     const uint8_t *q_fp4, const float *q_scale,
+                     const float *head_w, const uint8_t *k_fp4,
+                     const float *k_scale, const int32_t *cand_blocks,
+                     int32_t block, int32_t max_blocks, float *scores,
+                     int64_t ld, int32_t *d_err, csa2_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * a5, a7. Top-K selection   [CSA2] Hierarchical card; [D0] sec. 2.
+ *
+ * Per query, the k highest scores among its visible entries (cand_blocks ==
+ * NULL, row = entries 0 .. n_vis-1) or among its visible pool slots
+ * (cand_blocks != NULL, same slot map as csa2_index_score), by the total order
+ * (score descending, entry id ascending).  NaN and -inf are never selected.
+ *   idx   [Nq, k] selected ENTRY ids (pool slots are mapped back to entries);
+ *         the first count[q] are valid, in no particular order; the rest -1.
+ *   count [Nq]    min(k, number of eligible entries)
+ * Supported: 1 <= k <= 2048.
+ * ------------------------------------------------------------------------- */
+CSA2_API int csa2_topk(const csa2_batch *b, const float *scores, int64_t ld, int32_t k,
+              const int32_t *cand_blocks, int32_t block, int32_t max_blocks,
+              int32_t *idx, int32_t *count, int32_t *d_err,
+              csa2_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * a5, a6. Top-K plus hierarchical candidate blocks (L20-style source)
+ * [CSA2] Hierarchical card ("按 8 个一组归为 block ... 最多 2,048 个 block");
+ * [D0] sec. 2 (latest block always kept; no exclusion when everything fits).
+ *
+ * From full-visible scores (as csa2_index_score with cand_blocks == NULL):
+ *   idx/count as csa2_topk with cand_blocks == NULL;
+ *   blocks  [Nq, max_blocks]: with B = ceil(n_vis/block) blocks of `block`
+ *           consecutive entries and block score = max over the block's visible
+ *           entries (NaN ignored): all B blocks if B <= max_blocks, else block
+ *           B-1 (it holds the latest visible position) plus the max_blocks-1
+ *           best of blocks 0..B-2 by (block score desc, block id asc).  The
+ *           pool is a position budget: it always holds min(B, max_blocks)
+ *           blocks.  Ascending, -1 padded.
+ *   nblocks [Nq]
+ * Supported: 1 <= k <= 2048, block in [1, 64], max_blocks in [1, 4096].
+ * ------------------------------------------------------------------------- */
+CSA2_API int csa2_topk_candidates(const csa2_batch *b, const float *scores, int64_t ld,
+                         int32_t k, int32_t block, int32_t max_blocks,
+                         int32_t *idx, int32_t *count, int32_t *blocks,
+                         int32_t *nblocks, int32_t *d_err,
+                         csa2_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * a8-a10. Sparse + sliding-window attention under one softmax
+ * [D0] sec. 1 (own 128-token window plus at most 512 selected compressed
+ * positions per query); [CSA2] mixed-precision card (the 512-dim latent row is
+ * both key and value); [TAIL] sec. 2.3 (window lower bound).
+ *
+ * For query q (request r, position t) and head h:
+ *   rows = { KV row kv_start[r]+j : j in idx[q, 0:k], j >= 0 }
+ *        u { SWA row of position p : lo <= p <= t },
+ *   lo   = max(win_lo[q], t - window + 1, 0)     (win_lo NULL: 0)
+ *   l_i  = sm_scale * <Q[q,h,:], row_i>
+ *   out[q,h,:] = sum_i e^{l_i} row_i / (sum_i e^{l_i} + e^{sink[h]})
+ *   lse[q,h]   = ln(sum_i e^{l_i} + e^{sink[h]})          (sink NULL: no term)
+ * The union is not de-duplicated.  Reuse layers pass an earlier layer's idx:
+ * entries outside [0, n_vis(t)) or past kv_len are skipped and flagged
+ * (CSA2_DERR_RANGE_IDX); idx entries are expected to be distinct.  Window
+ * positions without a stored SWA row are skipped (CSA2_DERR_RANGE_WINDOW).  A
+ * query with no rows gets out = 0 and lse = -inf (or sink[h]).
+ *   q_bf16   [Nq, n_heads, dim] bf16;   out_bf16 [Nq, n_heads, dim] bf16
+ *   kv_fp8   [Nkv, dim] + kv_scale [Nkv, dim/32]: compressed KV pool
+ *   swa_fp8  [Nswa, dim] + swa_scale [Nswa, dim/32]: this layer's SWA rows
+ *   idx      [Nq, k] int32 or NULL (k ignored)
+ *   lse      [Nq, n_heads] fp32 or NULL
+ * Supported: dim == 512, n_heads in {16, 32, 64}, 0 <= k <= 2048,
+ * 1 <= window <= 1024.
+ * ------------------------------------------------------------------------- */
+CSA2_API int csa2_sparse_swa_attn(const csa2_batch *b, int32_t n_heads, int32_t dim,
+                         const void *q_bf16, const uint8_t *kv_fp8,
+                         const float *kv_scale, const int32_t *idx, int32_t k,
+                         const uint8_t *swa_fp8, const float *swa_scale,
+                         const int64_t *win_lo, int32_t window, float sm_scale,
+                         const float *sink, void *out_bf16, float *lse,
+                         int32_t *d_err, csa2_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA2_H_ */

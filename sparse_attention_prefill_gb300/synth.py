@@ -248,37 +248,36 @@ def full_layer(ctx: int, ratio: int, q_positions: List[int], n_heads: int, n_idx
                     _i64(q_positions, device), pool, {"full": L}, topk=topk, ld=entries)
 
 
-def decoder_replay(n_req: int, extend: int, prefix: int, n_heads: int, n_idx_heads: int,
+def decoder_replay(extends: List[int], prefixes: List[int], n_heads: int, n_idx_heads: int,
                    seed: int = 0, device="cpu", tag: str = "replay",
                    topk: int = TOPK, max_blocks: int = MAX_BLOCKS, block: int = BLOCK) -> Workload:
-    """``n_req`` requests, each an extend of ``extend`` tokens over ``prefix``
-    cached tokens (m = 1: one compressed entry per token).  The query rows are
-    each request's bounded-replay tail: the last min(128, extend) rows at their
-    absolute positions.  Layers: an L20-style source pass over those rows
-    (normal window, full-visible scoring, top-K and candidate pool), an
-    L21-style Reindex layer (pool-restricted scoring, tail window) and an
-    L22-style Reuse layer (tail window, the Reindex layer's indices)."""
-    seq = prefix + extend
-    tail = min(WINDOW, extend)
-    q_req, q_pos = [], []
+    """Requests r = 0.. each with an extend of ``extends[r]`` tokens over
+    ``prefixes[r]`` cached tokens (m = 1: one compressed entry per token).  The
+    query rows are each request's bounded-replay tail: the last
+    min(128, extend) rows at their absolute positions.  Layers: an L20-style
+    source pass over those rows (normal window, full-visible scoring, top-K and
+    candidate pool), an L21-style Reindex layer (pool-restricted scoring, tail
+    window) and an L22-style Reuse layer (tail window, the Reindex layer's
+    indices)."""
+    n_req = len(extends)
+    seqs = [p + e for p, e in zip(prefixes, extends)]
+    tails = [min(WINDOW, e) for e in extends]
+    q_req, q_pos, win = [], [], []
     for r in range(n_req):
-        q_req += [r] * tail
-        q_pos += list(range(seq - tail, seq))
-    pool = make_pool([seq] * n_req, seed, tag, device)
+        q_req += [r] * tails[r]
+        q_pos += list(range(seqs[r] - tails[r], seqs[r]))
+        win += [seqs[r] - tails[r]] * tails[r]
+    pool = make_pool(seqs, seed, tag, device)
     nq = len(q_pos)
-    src_lo = max(0, seq - tail - WINDOW + 1)
-    L20 = make_layer("L20", "source", nq, n_heads, n_idx_heads, [(src_lo, seq - src_lo)] * n_req,
-                     None, seed, tag, device, True)
-    win = [seq - tail] * nq
-    L21 = make_layer("L21", "reindex", nq, n_heads, n_idx_heads, [(seq - tail, tail)] * n_req,
-                     win, seed, tag, device, True)
-    L22 = make_layer("L22", "reuse", nq, n_heads, n_idx_heads, [(seq - tail, tail)] * n_req,
-                     win, seed, tag, device, False)
+    src = [(max(0, s - t - WINDOW + 1), s - max(0, s - t - WINDOW + 1)) for s, t in zip(seqs, tails)]
+    late = [(s - t, t) for s, t in zip(seqs, tails)]
+    L20 = make_layer("L20", "source", nq, n_heads, n_idx_heads, src, None, seed, tag, device, True)
+    L21 = make_layer("L21", "reindex", nq, n_heads, n_idx_heads, late, win, seed, tag, device, True)
+    L22 = make_layer("L22", "reuse", nq, n_heads, n_idx_heads, late, win, seed, tag, device, False)
     return Workload(tag, 1, n_heads, n_idx_heads, _i32(q_req, device), _i64(q_pos, device), pool,
                     {"L20": L20, "L21": L21, "L22": L22}, topk=topk, block=block,
-                    max_blocks=max_blocks,
-                    extend_len=_i32([extend] * n_req, device), seq_len=_i64([seq] * n_req, device),
-                    ld=seq)
+                    max_blocks=max_blocks, extend_len=_i32(extends, device),
+                    seq_len=_i64(seqs, device), ld=max(seqs))
 
 
 def hierarchical(ctx: int, nq: int, n_heads: int, n_idx_heads: int, seed: int = 0,
@@ -366,7 +365,7 @@ def config(name: str, device="cpu", seed: int = 0) -> Workload:
     if name == "c1_tiny_full":
         w = full_layer(4096, 2, list(range(3968, 4096)), 16, 8, seed, device, tag=name)
     elif name == "c2_decoder_replay":
-        w = decoder_replay(8, 8192, 0, 64, 32, seed, device, tag=name)
+        w = decoder_replay([8192] * 8, [0] * 8, 64, 32, seed, device, tag=name)
     elif name == "c3_encoder_prefill":
         w = full_layer(32768, 2, list(range(32768)), 64, 32, seed, device, tag=name)
     elif name == "c4_hierarchical":

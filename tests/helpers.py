@@ -1,0 +1,80 @@
+"""Test helpers: host copies of workloads for the oracle and parity metrics."""
+import numpy as np
+import torch
+
+from oracle import api as O
+
+
+def np_batch(b: dict) -> dict:
+    out = {}
+    for k, v in b.items():
+        out[k] = v.detach().cpu().numpy() if torch.is_tensor(v) else v
+    return out
+
+
+def npy(t):
+    if t is None:
+        return None
+    if t.dtype == torch.bfloat16:
+        return t.detach().cpu().view(torch.int16).numpy().view(np.uint16)
+    return t.detach().cpu().numpy()
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(bits.astype(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def attn_errors(gpu_bf16: torch.Tensor, ref_bits: np.ndarray):
+    g = gpu_bf16.detach().float().cpu().double().numpy()
+    r = bf16_to_f64(ref_bits)
+    d = np.abs(g - r)
+    return float(d.max() / max(np.abs(r).max(), 1e-30)), float(d.mean() / max(np.abs(r).mean(), 1e-30))
+
+
+ATTN_MAX_REL = 2e-2
+ATTN_MEAN_REL = 1e-3
+LSE_ABS = 1e-4
+
+
+def assert_attn_close(gpu_out, gpu_lse, ref_out, ref_lse):
+    mx, mean = attn_errors(gpu_out, ref_out)
+    assert mx <= ATTN_MAX_REL and mean <= ATTN_MEAN_REL, (mx, mean)
+    if ref_lse is not None and gpu_lse is not None:
+        gl = gpu_lse.detach().cpu().numpy()
+        fin = np.isfinite(ref_lse)
+        assert (np.isfinite(gl) == fin).all()
+        assert np.abs(gl[fin] - ref_lse[fin]).max(initial=0.0) <= LSE_ABS
+
+
+def topk_sets_match(gpu_idx, gpu_count, ref_idx, ref_count):
+    """Bit-exact comparison of selected sets (order within a row is free)."""
+    gi = gpu_idx.detach().cpu().numpy()
+    gc = gpu_count.detach().cpu().numpy()
+    assert (gc == ref_count).all(), np.nonzero(gc != ref_count)[0][:10]
+    for q in range(gi.shape[0]):
+        c = int(ref_count[q])
+        assert sorted(gi[q, :c].tolist()) == sorted(ref_idx[q, :c].tolist()), q
+        assert (gi[q, c:] == -1).all(), q
+
+
+def topk_near_tie_ok(gpu_idx, gpu_count, ref_idx, ref_count, ref_scores, entry_of_col=None,
+                     rel=1e-3):
+    """End-to-end top-K rule: sets equal except for swaps among entries whose
+    oracle scores lie within rel * |s_k| of the oracle's k-th score."""
+    gi = gpu_idx.detach().cpu().numpy()
+    gc = gpu_count.detach().cpu().numpy()
+    assert (gc == ref_count).all()
+    swaps = 0
+    for q in range(gi.shape[0]):
+        c = int(ref_count[q])
+        a, b = set(gi[q, :c].tolist()), set(ref_idx[q, :c].tolist())
+        diff = a ^ b
+        if not diff:
+            continue
+        row = ref_scores[q]
+        col = (lambda e: e) if entry_of_col is None else (lambda e: entry_of_col[q][e])
+        sk = min(row[col(e)] for e in b)
+        for e in diff:
+            assert abs(row[col(e)] - sk) <= rel * abs(sk) + 1e-30, (q, e, row[col(e)], sk)
+        swaps += len(diff) // 2
+    return swaps

@@ -1,0 +1,57 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds for
+sm_103a, loads, and exports exactly the entry points include/csa2.h declares;
+the product package never touches the oracle."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "csa2.h")).read()
+    return sorted(set(re.findall(r"CSA2_API\s+(?:const\s+char\s*\*|int)\s*(csa2_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_five_calls():
+    names = _declared()
+    for n in ("csa2_tail_layout", "csa2_index_score", "csa2_topk", "csa2_topk_candidates",
+              "csa2_sparse_swa_attn", "csa2_status_string"):
+        assert n in names
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    from sparse_attention_prefill_gb300 import build
+    path = build.build()
+    lib = ctypes.CDLL(path)
+    for n in _declared():
+        assert hasattr(lib, n), n
+    lib.csa2_status_string.restype = ctypes.c_char_p
+    assert lib.csa2_status_string(0) == b"ok"
+    # exported dynamic symbols are exactly the declared ones
+    out = os.popen("nm -D --defined-only %s" % path).read()
+    exported = sorted(set(re.findall(r" T (\w+)", out)))
+    assert exported == _declared()
+
+
+def test_host_validation_rejects_before_launch():
+    """Argument errors the host can see return a status without touching the GPU."""
+    from sparse_attention_prefill_gb300 import build
+    lib = ctypes.CDLL(build.build())
+    # negative request count, zero window
+    assert lib.csa2_tail_layout(-1, None, None, 128, None, None, None, None, None, None,
+                                ctypes.c_int64(0), None, None) == 1
+    assert lib.csa2_index_score(None, 32, 128, None, None, None, None, None, None, 8, 2048,
+                                None, ctypes.c_int64(0), None, None) == 1
+
+
+def test_product_package_does_not_use_the_oracle():
+    pkg = os.path.join(ROOT, "sparse_attention_prefill_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                txt = open(os.path.join(dirpath, f), encoding="utf8").read()
+                assert not re.search(r"^\s*(from|import)\s+oracle", txt, re.M), f
+                assert "csa2_oracle" not in txt, f
