@@ -233,7 +233,7 @@ def run_kernel_id():
     traffic is only reported for the kernel it was measured on."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("attn_tc.cu", "attn_simt.cu"):
+    for f in ("attn_tc.cu", "tcgen05.cuh"):
         p = os.path.join(ROOT, "sparse_attention_prefill_gb300", "csrc", f)
         if os.path.exists(p):
             h.update(open(p, "rb").read())

@@ -71,6 +71,7 @@ typedef struct CUstream_st *csa2_stream_t; /* same object as cudaStream_t */
 #define CSA2_DERR_LD 16           /* a score row longer than the row stride `ld` */
 #define CSA2_DERR_CAPACITY 32     /* tail rows beyond the output capacity */
 #define CSA2_DERR_BAD_EXTEND 64   /* an extend with E < 0 or S < E */
+#define CSA2_DERR_TIMEOUT 128     /* a pipeline wait inside a kernel gave up (internal error) */
 
 /* Rows of one layer call.  Host struct; every array is device memory.
  *   q_req[Nq]   request of each query row (0 <= q_req < num_req)

@@ -75,7 +75,7 @@ extern "C" CSA2_API int csa2_sparse_swa_attn(const csa2_batch *b, int32_t n_head
   if (n_heads != 16 && n_heads != 32 && n_heads != 64) return CSA2_ERR_UNSUPPORTED;
   if (k > 2048 || window > 1024) return CSA2_ERR_UNSUPPORTED;
   const csa2::Batch v = csa2::to_device_view(b);
-  return csa2::attn_simt(v, n_heads, reinterpret_cast<const __nv_bfloat16 *>(q_bf16), kv_fp8,
+  return csa2::attn_tc(v, n_heads, reinterpret_cast<const __nv_bfloat16 *>(q_bf16), kv_fp8,
                          kv_scale, idx, k, swa_fp8, swa_scale, win_lo, window, sm_scale, sink,
                          reinterpret_cast<__nv_bfloat16 *>(out_bf16), lse, d_err,
                          csa2::as_stream(stream));

@@ -1,0 +1,676 @@
+// a8-a10 on the 5th-generation tensor cores: sparse + sliding-window attention
+// under one softmax, FP8 block-32 rows dequantised to f16 in shared memory,
+// tcgen05 MMAs accumulating in TMEM.
+//
+// What is computed (SGLang/Miles day-0 article sec. 1; "DeepSeek V4.1 Flash
+// 建模" mixed-precision card: the 512-dim latent row is key and value; window
+// lower bound: "SGLang 如何让 DeepSeek V4.1 Flash 的后半层只处理尾部 token" sec. 2.3):
+//   rows(q) = selected compressed rows  u  window rows [lo, t]
+//   O[q,h]  = softmax_i(sm_scale <Q[q,h], row_i>) . rows
+//
+// Formulation.  A query has H <= 64 heads (zero-padded to 64) and up to
+// k + window rows of 512 channels.  Rows are processed in chunks of 128 and
+// every product is written transposed so that the MMA M dimension is 128:
+//   S^T[r, h] = sum_d R[r, d] Q[h, d]          (M = 128 rows,  N = 64, K = 512)
+//   O^T[d, h] += sum_r R[r, d] P[r, h]         (M = 128 chans, N = 64, K = 128; 4 tiles)
+// One f16 copy of the chunk R (SW128 layout, 8 column blocks of 64 channels)
+// is the K-major A operand of the first product and the MN-major A operand of
+// the second.  S^T is double-buffered in TMEM (2 x 64 columns), O^T occupies
+// 4 x 64 columns.  The softmax runs online with a lazily updated reference
+// maximum per head: it is only moved (and O^T and the row sums rescaled) when
+// a logit exceeds it by more than 2^8, so P <= 256 always fits f16.
+//
+// Roles (16 warps, one CTA per SM, persistent over queries):
+//   warps 0-7   softmax + epilogue; warp w owns TMEM lanes 32*(w%4).. (rows of
+//               S^T / channels of O^T) and heads 32*(w/4) .. +31
+//   warp 8      TMEM allocation; lane 0 issues every MMA and commit
+//   warps 9-15  producers: Q (bf16 -> f16), row gather + E4M3 -> f16 dequant,
+//               in 4 pipeline steps of 128 channels per chunk
+// Every wait is bounded (about two seconds); on expiry the kernel raises
+// CSA2_DERR_TIMEOUT, drains and returns.
+#include "common.cuh"
+#include "kernels.cuh"
+#include "tcgen05.cuh"
+
+namespace csa2 {
+namespace {
+
+using namespace tc;
+
+constexpr int kDim = 512;
+constexpr int kRowsPerChunk = 128;
+constexpr int kHeadsPad = 64;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kMmaWarp = 8;
+constexpr int kProducerWarp0 = 9;
+constexpr int kProducerWarps = 7;
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+constexpr int kProducerThreads = kProducerWarps * 32;
+constexpr int kMaxSel = 2048;
+
+// shared-memory map (bytes)
+constexpr uint32_t kOffR = 0;           // 8 blocks x [128 rows x 128 B]  (128 KB)
+constexpr uint32_t kRBlock = 16384;
+constexpr uint32_t kOffQ = 131072;      // 8 blocks x [64 heads x 128 B]  (64 KB)
+constexpr uint32_t kQBlock = 8192;
+constexpr uint32_t kOffP = 196608;      // [128 rows x 64 heads] f16       (16 KB)
+constexpr uint32_t kOffList = 212992;   // int32 [kMaxSel]                 (8 KB)
+constexpr uint32_t kOffMisc = 221184;
+constexpr uint32_t kSmemBytes = kOffMisc + 2048;
+
+// TMEM columns
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;           // 2 x 64
+constexpr uint32_t kColO = 128;         // 4 x 64
+
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kDerrTimeout = 128;
+
+struct Misc {
+  uint64_t q_full, q_empty, s_full[2], s_empty[2], p_full, p_empty, o_full, o_empty, done;
+  uint64_t r_full[4], r_empty[4];
+  uint64_t sm_grp, pr_grp;  // group syncs of the softmax warps / the producer warps
+  uint32_t tmem_base;
+  int abort;
+  int votes[2][8];      // softmax warps: "a logit exceeded the reference", by chunk parity
+  float m_ref[64];      // reference maximum per head (log2 units)
+  float alpha[64];      // rescale factors of the current slow path
+  float red[4][64];     // cross-warp reductions
+  int nsel;             // producers: valid selected rows of the current query
+};
+static_assert(sizeof(Misc) <= 2048, "misc region");
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait; on expiry raise the abort flag and report false.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Misc *ms) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*(volatile int *)&ms->abort) return false;
+    if (globaltimer() - t0 > kWaitNs) {
+      atomicExch(&ms->abort, 1);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Group barrier among the warps of one role, on an mbarrier whose arrival
+// count is the role's warp count: bounded and abort-aware, unlike bar.sync.
+__device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &phase, Misc *ms) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+  const bool ok = wait_bar(bar, phase & 1, ms);
+  ++phase;
+  return ok;
+}
+
+struct Rows {
+  int64_t nsel;        // valid selected rows
+  int64_t win_first;   // SWA row of the first window row
+  int64_t nwin;        // window rows
+  int err;
+};
+
+// Rows of query q, computed cooperatively by one full warp (every lane gets
+// the result).  When `list` is given, the valid selected entries are
+// compacted into it in idx order.
+__device__ Rows query_rows(const Batch &b, int q, const int32_t *__restrict__ idx, int k,
+                           const int64_t *__restrict__ win_lo, int window, int *list) {
+  const int lane = threadIdx.x & 31;
+  const int r = b.q_req[q];
+  const int64_t t = b.q_pos[q];
+  const int64_t n_vis = n_visible(t, b.ratio);
+  const int64_t kvn = b.kv_len[r];
+  Rows o;
+  o.err = 0;
+  int64_t cnt = 0;
+  for (int i0 = 0; i0 < k; i0 += 32) {
+    const int i = i0 + lane;
+    int64_t j = -1;
+    if (i < k) j = idx[(int64_t)q * k + i];
+    const bool bad = j >= 0 && (j >= n_vis || j >= kvn);
+    const bool ok = j >= 0 && !bad;
+    if (__any_sync(0xffffffffu, bad)) o.err |= CSA2_DERR_RANGE_IDX;
+    const uint32_t m = __ballot_sync(0xffffffffu, ok);
+    if (list && ok) list[cnt + __popc(m & ((1u << lane) - 1u))] = (int)j;
+    cnt += __popc(m);
+  }
+  o.nsel = cnt;
+  int64_t lo = t - window + 1;
+  if (win_lo && win_lo[q] > lo) lo = win_lo[q];
+  if (lo < 0) lo = 0;
+  const int64_t p0 = b.swa_pos0[r], pn = b.swa_len[r];
+  int64_t lo_v = lo > p0 ? lo : p0;
+  int64_t hi_v = t < p0 + pn - 1 ? t : p0 + pn - 1;
+  if (lo <= t && (lo < p0 || t > p0 + pn - 1)) o.err |= CSA2_DERR_RANGE_WINDOW;
+  o.nwin = hi_v >= lo_v ? hi_v - lo_v + 1 : 0;
+  o.win_first = b.swa_start[r] + (lo_v - p0);
+  return o;
+}
+
+__device__ __forceinline__ int n_chunks_of(int64_t nrows) {
+  const int64_t c = (nrows + kRowsPerChunk - 1) / kRowsPerChunk;
+  return c > 0 ? (int)c : 1;
+}
+
+struct Params {
+  Batch b;
+  int n_heads;
+  const __nv_bfloat16 *q;
+  const uint8_t *kv_fp8;
+  const float *kv_scale;
+  const int32_t *idx;
+  int k;
+  const uint8_t *swa_fp8;
+  const float *swa_scale;
+  const int64_t *win_lo;
+  int window;
+  float scale_log2;
+  const float *sink;
+  __nv_bfloat16 *out;
+  float *lse;
+  int32_t *d_err;
+};
+
+// ---------------------------------------------------------------------------
+// producers
+// ---------------------------------------------------------------------------
+struct Item {
+  uint4 codes;
+  float scale;
+};
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, __half2 s) {
+  __half2 x = *reinterpret_cast<__half2 *>(&a);
+  x = __hmul2(x, s);
+  return *reinterpret_cast<uint32_t *>(&x);
+}
+
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two) {
+  uint32_t h2;
+  const uint16_t v = (uint16_t)two;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+  return h2;
+}
+
+// one pipeline step: channels [128*pair, 128*pair+128) of the 128 rows of a chunk
+constexpr int kItemsPerStep = kRowsPerChunk * 8;  // 8 segments of 16 channels per row
+constexpr int kItemsPerThread = (kItemsPerStep + kProducerThreads - 1) / kProducerThreads;
+
+__device__ __forceinline__ void load_step(const Params &P, const int *list, const Rows &rows,
+                                          int64_t kv0, int chunk, int pair, int ptid,
+                                          Item (&it)[kItemsPerThread]) {
+#pragma unroll
+  for (int i = 0; i < kItemsPerThread; ++i) {
+    const int item = ptid + i * kProducerThreads;
+    it[i].codes = make_uint4(0, 0, 0, 0);
+    it[i].scale = 0.f;
+    if (item < kItemsPerStep) {
+      const int row = item >> 3, seg = item & 7;
+      const int64_t ri = (int64_t)chunk * kRowsPerChunk + row;
+      const int d = pair * 128 + seg * 16;
+      const uint8_t *src = nullptr;
+      const float *sc = nullptr;
+      if (ri < rows.nsel) {
+        const int64_t g = kv0 + list[ri];
+        src = P.kv_fp8 + g * kDim;
+        sc = P.kv_scale + g * (kDim / 32);
+      } else if (ri < rows.nsel + rows.nwin) {
+        const int64_t g = rows.win_first + (ri - rows.nsel);
+        src = P.swa_fp8 + g * kDim;
+        sc = P.swa_scale + g * (kDim / 32);
+      }
+      if (src) {
+        it[i].codes = __ldg(reinterpret_cast<const uint4 *>(src + d));
+        it[i].scale = __ldg(sc + d / 32);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void store_step(uint8_t *R, int pair, int ptid,
+                                           const Item (&it)[kItemsPerThread]) {
+#pragma unroll
+  for (int i = 0; i < kItemsPerThread; ++i) {
+    const int item = ptid + i * kProducerThreads;
+    if (item < kItemsPerStep) {
+      const int row = item >> 3, seg = item & 7;
+      const int d = pair * 128 + seg * 16;
+      const __half2 s2 = __float2half2_rn(it[i].scale);
+      const uint32_t w[4] = {it[i].codes.x, it[i].codes.y, it[i].codes.z, it[i].codes.w};
+      uint32_t h[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        h[2 * j] = hmul2_u32(e4m3x2_f16x2(w[j] & 0xffffu), s2);
+        h[2 * j + 1] = hmul2_u32(e4m3x2_f16x2(w[j] >> 16), s2);
+      }
+      *reinterpret_cast<uint4 *>(R + sw128_offset(row, d, kRBlock)) =
+          make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4 *>(R + sw128_offset(row, d + 8, kRBlock)) =
+          make_uint4(h[4], h[5], h[6], h[7]);
+    }
+  }
+}
+
+__device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms) {
+  const int ptid = threadIdx.x - kProducerWarp0 * 32;
+  const int lane = threadIdx.x & 31;
+  uint8_t *R = smem + kOffR;
+  uint8_t *Qs = smem + kOffQ;
+  int *list = reinterpret_cast<int *>(smem + kOffList);
+  int err = 0;
+  uint32_t g = 0;  // chunks produced by this CTA
+  uint32_t qi = 0, gp = 0;
+  for (int q = blockIdx.x; q < P.b.num_q; q += gridDim.x, ++qi) {
+    // ---- Q of this query (f16, heads zero-padded to 64)
+    if (!wait_bar(&ms->q_empty, (qi & 1) ^ 1, ms)) break;
+    const __nv_bfloat16 *qg = P.q + (int64_t)q * P.n_heads * kDim;
+#pragma unroll 4
+    for (int it = ptid; it < kHeadsPad * (kDim / 8); it += kProducerThreads) {
+      const int h = it / (kDim / 8), d = (it % (kDim / 8)) * 8;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (h < P.n_heads) {
+        const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(qg + (int64_t)h * kDim + d));
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xffff0000u);
+          __half2 hh = __floats2half2_rn(lo, hi);
+          o[j] = *reinterpret_cast<uint32_t *>(&hh);
+        }
+        v = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      *reinterpret_cast<uint4 *>(Qs + sw128_offset(h, d, kQBlock)) = v;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ms->q_full);
+    // ---- row list (first producer warp), shared with the other producers
+    Rows rows{0, 0, 0, 0};
+    if (threadIdx.x / 32 == kProducerWarp0) {
+      rows = query_rows(P.b, q, P.idx, P.k, P.win_lo, P.window, list);
+      err |= rows.err;
+      if (lane == 0) ms->nsel = (int)rows.nsel;
+    }
+    if (!group_sync(&ms->pr_grp, gp, ms)) break;
+    {
+      // every producer recomputes the window part (cheap) and reads nsel
+      Rows r2 = query_rows(P.b, q, nullptr, 0, P.win_lo, P.window, nullptr);
+      rows.nwin = r2.nwin;
+      rows.win_first = r2.win_first;
+      rows.nsel = ms->nsel;
+    }
+    const int64_t kv0 = P.b.kv_start[P.b.q_req[q]];
+    const int nch = n_chunks_of(rows.nsel + rows.nwin);
+    // ---- chunks: 4 steps of 128 channels each, loads issued before the wait
+    Item cur[kItemsPerThread], nxt[kItemsPerThread];
+    load_step(P, list, rows, kv0, 0, 0, ptid, cur);
+    bool ok = true;
+    for (int c = 0; c < nch && ok; ++c, ++g) {
+#pragma unroll 1
+      for (int pair = 0; pair < 4; ++pair) {
+        const int nc = pair == 3 ? c + 1 : c, np = (pair + 1) & 3;
+        if (nc < nch) load_step(P, list, rows, kv0, nc, np, ptid, nxt);
+        if (!wait_bar(&ms->r_empty[pair], (g & 1) ^ 1, ms)) {
+          ok = false;
+          break;
+        }
+        store_step(R, pair, ptid, cur);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ms->r_full[pair]);
+#pragma unroll
+        for (int i = 0; i < kItemsPerThread; ++i) cur[i] = nxt[i];
+      }
+    }
+    if (!ok) break;
+    if (!group_sync(&ms->pr_grp, gp, ms)) break;  // the list is rebuilt for the next query
+  }
+  if (threadIdx.x / 32 == kProducerWarp0) {
+    err = __reduce_or_sync(0xffffffffu, err);
+    if (lane == 0) raise_err(P.d_err, err);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// MMA issuer: the whole warp walks the queries (row counts need the warp),
+// lane 0 waits on the barriers and issues every MMA and commit.
+// ---------------------------------------------------------------------------
+__device__ void mma_role(const Params &P, uint8_t *smem, Misc *ms) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t tmem = ms->tmem_base;
+  const uint32_t r0 = smem_u32(smem + kOffR), q0 = smem_u32(smem + kOffQ),
+                 p0 = smem_u32(smem + kOffP);
+  const uint32_t id_s = make_idesc_f16(128, kHeadsPad, false, false);
+  const uint32_t id_o = make_idesc_f16(128, kHeadsPad, true, true);
+  uint32_t g = 0, qi = 0;
+  int ok = 1;
+  for (int q = blockIdx.x; q < P.b.num_q; q += gridDim.x, ++qi) {
+    const Rows rows = query_rows(P.b, q, P.idx, P.k, P.win_lo, P.window, nullptr);
+    const int nch = n_chunks_of(rows.nsel + rows.nwin);
+    if (lane == 0) {
+      for (int c = 0; c < nch && ok; ++c, ++g) {
+        const uint32_t sb = g & 1;
+        const uint32_t s_tmem = tmem + kColS + sb * 64;
+        // ---- S^T(c) = R . Q^T into S buffer sb
+        ok = wait_bar(&ms->s_empty[sb], ((g >> 1) & 1) ^ 1, ms);
+        if (ok && c == 0) ok = wait_bar(&ms->q_full, qi & 1, ms);
+        for (int pair = 0; pair < 4 && ok; ++pair) {
+          ok = wait_bar(&ms->r_full[pair], g & 1, ms);
+          if (!ok) break;
+          fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const int blk = pair * 2 + (kk >> 2);
+            const uint64_t a = make_desc_sw128(r0 + blk * kRBlock + (kk & 3) * 32, 16, 1024);
+            const uint64_t bq = make_desc_sw128(q0 + blk * kQBlock + (kk & 3) * 32, 16, 1024);
+            mma_f16(s_tmem, a, bq, id_s, (pair > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        if (!ok) break;
+        mma_commit(&ms->s_full[sb]);
+        if (c == nch - 1) mma_commit(&ms->q_empty);
+        // ---- O^T += R^T . P^T, 4 tiles of 128 channels
+        ok = wait_bar(&ms->p_full, g & 1, ms);
+        if (ok && c == 0) ok = wait_bar(&ms->o_empty, (qi & 1) ^ 1, ms);
+        if (!ok) break;
+        fence_after_sync();
+        for (int t = 0; t < 4; ++t) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint64_t a = make_desc_sw128(r0 + t * 2 * kRBlock + ks * 2048, kRBlock, 1024);
+            const uint64_t bp = make_desc_sw128(p0 + ks * 2048, kRBlock, 1024);
+            mma_f16(tmem + kColO + t * 64, a, bp, id_o, (c > 0 || ks > 0) ? 1u : 0u);
+          }
+          mma_commit(&ms->r_empty[t]);
+        }
+        mma_commit(&ms->p_empty);
+        if (c == nch - 1) mma_commit(&ms->o_full);
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) break;
+  }
+  // drain: every MMA issued so far has completed once `done` flips (bounded
+  // by time only, so that TMEM is never freed under a running MMA)
+  if (lane == 0) {
+    mma_commit(&ms->done);
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(&ms->done, 0) && globaltimer() - t0 < kWaitNs) {
+    }
+  }
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// softmax + epilogue (warps 0-7)
+// ---------------------------------------------------------------------------
+__device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sp = warp & 3;          // TMEM sub-partition: lanes 32*sp ..
+  const int hh = warp >> 2;         // head half: heads 32*hh ..
+  const int stid = threadIdx.x;     // 0..255
+  const uint32_t tmem = ms->tmem_base;
+  const uint32_t lane_addr = (uint32_t)(32 * sp) << 16;
+  uint8_t *Pbuf = smem + kOffP;
+  const float NEG_INF = -INFINITY;
+  float lsum[32];
+  uint32_t g = 0, qi = 0, gp = 0;
+  bool ok = true;
+  if (stid < 64) ms->m_ref[stid] = NEG_INF;
+  ok = group_sync(&ms->sm_grp, gp, ms);
+  for (int q = blockIdx.x; q < P.b.num_q && ok; q += gridDim.x, ++qi) {
+    const Rows rows = query_rows(P.b, q, P.idx, P.k, P.win_lo, P.window, nullptr);
+    const int64_t nrows = rows.nsel + rows.nwin;
+    const int nch = n_chunks_of(nrows);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) lsum[j] = 0.f;
+    for (int c = 0; c < nch; ++c, ++g) {
+      const uint32_t sb = g & 1;
+      ok = wait_bar(&ms->s_full[sb], (g >> 1) & 1, ms);
+      if (!ok) break;
+      fence_after_sync();
+      uint32_t v[32];
+      tmem_ld32x32b_x32(tmem + lane_addr + kColS + sb * 64 + 32 * hh, v);
+      tmem_wait_ld();
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ms->s_empty[sb]);
+      const int64_t row = (int64_t)c * kRowsPerChunk + 32 * sp + lane;
+      const bool valid = row < nrows;
+      float x[32];
+      bool exceed = false;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        x[j] = valid ? __uint_as_float(v[j]) * P.scale_log2 : NEG_INF;
+        exceed |= x[j] > ms->m_ref[32 * hh + j] + 8.f;
+      }
+      // does any logit of the chunk exceed its head's reference by 2^8?
+      const int vb = g & 1;
+      const bool vote = __any_sync(0xffffffffu, exceed);
+      if (lane == 0) ms->votes[vb][warp] = vote ? 1 : 0;
+      if (!(ok = group_sync(&ms->sm_grp, gp, ms))) break;
+      bool slow = false;
+#pragma unroll
+      for (int w = 0; w < kSoftmaxWarps; ++w) slow |= ms->votes[vb][w] != 0;
+      if (slow) {
+        // per-head maximum over the chunk's 128 rows: transposed butterfly in
+        // the warp (lane j ends with head 32*hh + j), then across the 4 warps
+        float y[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) y[j] = x[j];
+#pragma unroll
+        for (int w = 16; w >= 1; w >>= 1) {
+          const bool upper = (lane & w) != 0;
+#pragma unroll
+          for (int j = 0; j < w; ++j) {
+            const float send = upper ? y[j] : y[j + w];
+            const float keep = upper ? y[j + w] : y[j];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, w);
+            y[j] = fmaxf(keep, recv);
+          }
+        }
+        ms->red[sp][32 * hh + lane] = y[0];
+        if (!(ok = group_sync(&ms->sm_grp, gp, ms))) break;
+        if (stid < 64) {
+          const float old = ms->m_ref[stid];
+          float mx = fmaxf(fmaxf(ms->red[0][stid], ms->red[1][stid]),
+                           fmaxf(ms->red[2][stid], ms->red[3][stid]));
+          mx = fmaxf(mx, old);
+          ms->alpha[stid] = (old == NEG_INF) ? 0.f : exp2f(old - mx);
+          ms->m_ref[stid] = mx;
+        }
+        if (!(ok = group_sync(&ms->sm_grp, gp, ms))) break;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) lsum[j] *= ms->alpha[32 * hh + j];
+      }
+      // P(c) may be written once O^T(c-1) has consumed P(c-1); that also
+      // means every earlier O^T MMA has completed (needed for a rescale)
+      ok = wait_bar(&ms->p_empty, (g & 1) ^ 1, ms);
+      if (!ok) break;
+      fence_after_sync();
+      if (slow && c > 0) {
+        for (int t = 0; t < 4; ++t) {
+          uint32_t o[32];
+          const uint32_t a = tmem + lane_addr + kColO + t * 64 + 32 * hh;
+          tmem_ld32x32b_x32(a, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            o[j] = __float_as_uint(__uint_as_float(o[j]) * ms->alpha[32 * hh + j]);
+          tmem_st32x32b_x32(a, o);
+        }
+        tmem_wait_st();
+      }
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const float m0 = ms->m_ref[32 * hh + j], m1 = ms->m_ref[32 * hh + j + 1];
+        const float p0 = exp2f(x[j] - (m0 == NEG_INF ? 0.f : m0));
+        const float p1 = exp2f(x[j + 1] - (m1 == NEG_INF ? 0.f : m1));
+        lsum[j] += p0;
+        lsum[j + 1] += p1;
+        __half2 h2 = __floats2half2_rn(p0, p1);
+        pk[j / 2] = *reinterpret_cast<uint32_t *>(&h2);
+      }
+      const int prow = 32 * sp + lane;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<uint4 *>(Pbuf + sw128_offset(prow, 32 * hh + 8 * i, 0)) =
+            make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      fence_proxy_async_smem();
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ms->p_full);
+    }
+    if (!ok) break;
+    // ---- epilogue: row sums, normalisation, bf16 output, lse
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+      const bool upper = (lane & w) != 0;
+#pragma unroll
+      for (int j = 0; j < w; ++j) {
+        const float send = upper ? lsum[j] : lsum[j + w];
+        const float keep = upper ? lsum[j + w] : lsum[j];
+        lsum[j] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+      }
+    }
+    ms->red[sp][32 * hh + lane] = lsum[0];
+    if (!(ok = group_sync(&ms->sm_grp, gp, ms))) break;
+    if (stid < 64) {
+      float l = (ms->red[0][stid] + ms->red[1][stid]) + (ms->red[2][stid] + ms->red[3][stid]);
+      const float m = ms->m_ref[stid];
+      const float mu = m == NEG_INF ? 0.f : m;
+      if (P.sink && stid < P.n_heads) l += exp2f(P.sink[stid] * 1.4426950408889634f - mu);
+      ms->alpha[stid] = l > 0.f ? 1.f / l : 0.f;
+      if (P.lse && stid < P.n_heads)
+        P.lse[(int64_t)q * P.n_heads + stid] =
+            l > 0.f ? (mu + log2f(l)) * 0.6931471805599453f : NEG_INF;
+      ms->m_ref[stid] = NEG_INF;   // reference of the next query
+    }
+    if (!(ok = group_sync(&ms->sm_grp, gp, ms))) break;
+    ok = wait_bar(&ms->o_full, qi & 1, ms);
+    if (!ok) break;
+    fence_after_sync();
+    __nv_bfloat16 *og = P.out + (int64_t)q * P.n_heads * kDim;
+    for (int t = 0; t < 4; ++t) {
+      uint32_t o[32];
+      tmem_ld32x32b_x32(tmem + lane_addr + kColO + t * 64 + 32 * hh, o);
+      tmem_wait_ld();
+      const int d = t * 128 + 32 * sp + lane;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int h = 32 * hh + j;
+        if (h < P.n_heads)
+          og[(int64_t)h * kDim + d] = __float2bfloat16_rn(__uint_as_float(o[j]) * ms->alpha[h]);
+      }
+    }
+    fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ms->o_empty);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(Params P) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Misc *ms = reinterpret_cast<Misc *>(smem + kOffMisc);
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    mbar_init(&ms->q_full, kProducerWarps);
+    mbar_init(&ms->q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ms->s_full[i], 1);
+      mbar_init(&ms->s_empty[i], kSoftmaxWarps);
+    }
+    mbar_init(&ms->p_full, kSoftmaxWarps);
+    mbar_init(&ms->p_empty, 1);
+    mbar_init(&ms->o_full, 1);
+    mbar_init(&ms->o_empty, kSoftmaxWarps);
+    mbar_init(&ms->done, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&ms->r_full[i], kProducerWarps);
+      mbar_init(&ms->r_empty[i], 1);
+    }
+    mbar_init(&ms->sm_grp, kSoftmaxWarps);
+    mbar_init(&ms->pr_grp, kProducerWarps);
+    ms->abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&ms->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp < kSoftmaxWarps) {
+    softmax_role(P, smem, ms);
+  } else if (warp == kMmaWarp) {
+    mma_role(P, smem, ms);
+  } else {
+    producer_role(P, smem, ms);
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (ms->abort && threadIdx.x == 0) raise_err(P.d_err, kDerrTimeout);
+  if (warp == kMmaWarp) {
+    fence_after_sync();
+    tmem_dealloc(ms->tmem_base, kTmemCols);
+  }
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
+}
+
+}  // namespace
+
+int attn_tc(const Batch &b, int n_heads, const __nv_bfloat16 *q, const uint8_t *kv_fp8,
+            const float *kv_scale, const int32_t *idx, int k, const uint8_t *swa_fp8,
+            const float *swa_scale, const int64_t *win_lo, int window, float sm_scale,
+            const float *sink, __nv_bfloat16 *out, float *lse, int32_t *d_err,
+            cudaStream_t st) {
+  if (b.num_q == 0) return CSA2_OK;
+  if (n_heads > kHeadsPad || k > kMaxSel) return CSA2_ERR_UNSUPPORTED;
+  Params P;
+  P.b = b;
+  P.n_heads = n_heads;
+  P.q = q;
+  P.kv_fp8 = kv_fp8;
+  P.kv_scale = kv_scale;
+  P.idx = idx;
+  P.k = idx ? k : 0;
+  P.swa_fp8 = swa_fp8;
+  P.swa_scale = swa_scale;
+  P.win_lo = win_lo;
+  P.window = window;
+  P.scale_log2 = sm_scale * 1.4426950408889634f;
+  P.sink = sink;
+  P.out = out;
+  P.lse = lse;
+  P.d_err = d_err;
+  cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)kSmemBytes);
+  const int grid = b.num_q < sm_count() ? b.num_q : sm_count();
+  attn_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(P);
+  return launch_status();
+}
+
+}  // namespace csa2

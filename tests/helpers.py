@@ -33,7 +33,13 @@ def attn_errors(gpu_bf16: torch.Tensor, ref_bits: np.ndarray):
 
 ATTN_MAX_REL = 2e-2
 ATTN_MEAN_REL = 1e-3
-LSE_ABS = 1e-4
+# lse = ln sum_i e^{l_i}: its error is the softmax-weighted mean of the logit
+# errors.  With f16 operands (dequantised rows and f16 scales: <= 2^-10
+# relative per element) one unit-variance logit over 512 channels errs by
+# sigma ~ 2^-11 * sm_scale * ||q o r||_2 ~ 5e-4 (less when many rows share the
+# weight).  Bounds: 4 sigma for the worst element, sigma / 2 on average.
+LSE_ABS_MAX = 2e-3
+LSE_ABS_MEAN = 2.5e-4
 
 
 def assert_attn_close(gpu_out, gpu_lse, ref_out, ref_lse):
@@ -43,7 +49,9 @@ def assert_attn_close(gpu_out, gpu_lse, ref_out, ref_lse):
         gl = gpu_lse.detach().cpu().numpy()
         fin = np.isfinite(ref_lse)
         assert (np.isfinite(gl) == fin).all()
-        assert np.abs(gl[fin] - ref_lse[fin]).max(initial=0.0) <= LSE_ABS
+        d = np.abs(gl[fin] - ref_lse[fin])
+        if d.size:
+            assert d.max() <= LSE_ABS_MAX and d.mean() <= LSE_ABS_MEAN, (d.max(), d.mean())
 
 
 def topk_sets_match(gpu_idx, gpu_count, ref_idx, ref_count):
