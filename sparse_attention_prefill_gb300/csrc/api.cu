@@ -28,8 +28,8 @@ extern "C" CSA2_API int csa2_index_score(const csa2_batch *b, int32_t n_heads, i
   if (n_heads != 8 && n_heads != 16 && n_heads != 32 && n_heads != 64) return CSA2_ERR_UNSUPPORTED;
   if (cand_blocks && (block > 64 || max_blocks > 4096)) return CSA2_ERR_UNSUPPORTED;
   const csa2::Batch v = csa2::to_device_view(b);
-  return csa2::index_score_simt(v, n_heads, q_fp4, q_scale, head_w, k_fp4, k_scale, cand_blocks,
-                                block, max_blocks, scores, ld, d_err, csa2::as_stream(stream));
+  return csa2::index_score_tc(v, n_heads, q_fp4, q_scale, head_w, k_fp4, k_scale, cand_blocks,
+                              block, max_blocks, scores, ld, d_err, csa2::as_stream(stream));
 }
 
 extern "C" CSA2_API int csa2_topk(const csa2_batch *b, const float *scores, int64_t ld, int32_t k,

@@ -1,0 +1,479 @@
+// a2-a4, a7 on the 5th-generation tensor cores: index scores
+//
+//   s(q, j) = sum_h w[q,h] * max(0, <Qi[q,h], Ki[j]>)
+//
+// ("DeepSeek V4.1 Flash 建模", CSA2 and Hierarchical Sparse Indexer cards;
+// SGLang/Miles day-0 article sec. 5: an MQA-shaped indexer over the FP4 keys
+// of the nearest KV source, heads replicated.)
+//
+// Formulation.  The contraction is written with the keys as the MMA M
+// dimension and (query, head) pairs as N:
+//   D[j, (q,h)] = sum_d K[j, d] Qi[q, h, d]     (M = 128 keys, N <= 256, K = 128)
+// so that the head reduction is a per-thread loop in the epilogue: thread j
+// reads its TMEM lane (key j) and sums w[q,h] * ReLU(D[j, (q,h)]) over the
+// head columns of query q.  MXFP4 operands are dequantised to f16 in shared
+// memory: an E2M1 value times a power-of-two scale is exact in f16 (for
+// scales in [2^-23, 2^12]) and f16 products accumulate exactly in fp32, so the
+// per-head dots are exact; only the fp32 head sum rounds.
+//
+// Work unit (one CTA): a tile of 256/Hi consecutive query rows and a chunk of
+// 16 key tiles (2048 keys or pool slots).  Rows of the tile that belong to the
+// same request share key tiles ("runs", full mode); in pool mode every query
+// has its own slot list and is its own run.  Roles (12 warps):
+//   warps 0-7   epilogue (warp w: TMEM lanes 32*(w%4).., queries of parity w/4)
+//   warp 8      TMEM allocation; lane 0 issues the MMAs
+//   warps 9-11  producers: key gather + E2M1 -> f16 into a 4-stage ring
+// Waits are time-bounded (CSA2_DERR_TIMEOUT on expiry).
+#include "common.cuh"
+#include "kernels.cuh"
+#include "tcgen05.cuh"
+
+namespace csa2 {
+namespace {
+
+using namespace tc;
+
+constexpr int kKeyTile = 128;
+constexpr int kTilesPerChunk = 16;
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kMmaWarp = 8;
+constexpr int kProdWarp0 = 9;
+constexpr int kProdWarps = 3;
+constexpr int kWarps = 12;
+constexpr int kThreads = kWarps * 32;
+constexpr int kProdThreads = kProdWarps * 32;
+constexpr int kBRows = 256 + 16;       // (query, head) rows + padding for N rounding
+
+constexpr uint32_t kABlock = kKeyTile * 128;           // 16 KB: one 64-column block
+constexpr uint32_t kAStage = 2 * kABlock;              // 32 KB: 128 keys x 128 f16
+constexpr uint32_t kBBlock = kBRows * 128;             // 34 KB
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffB = kOffA + kStages * kAStage;  // 128 KB
+constexpr uint32_t kOffMisc = kOffB + 2 * kBBlock;     // +68 KB
+constexpr uint32_t kSmemBytes = kOffMisc + 4096;
+
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kDerrTimeout = 128;
+constexpr int kMaxQT = 32;
+
+struct RunInfo {
+  int ql0, nq, req;
+  int64_t len;  // longest row of the run
+};
+
+struct Misc {
+  uint64_t a_full[kStages], a_empty[kStages], d_full[2], d_empty[2], done;
+  uint32_t tmem_base;
+  int abort;
+  int nruns;
+  RunInfo runs[kMaxQT];
+  int64_t row_len[kMaxQT];   // per query of the tile (0 past the batch)
+  int64_t n_vis[kMaxQT];
+  float w[256];              // head weights of the tile
+};
+static_assert(sizeof(Misc) <= 4096, "misc");
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Misc *ms) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*(volatile int *)&ms->abort) return false;
+    if (globaltimer() - t0 > kWaitNs) {
+      atomicExch(&ms->abort, 1);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ bool mx_scale_ok(float s) {
+  const uint32_t u = __float_as_uint(s);
+  const int e = (int)((u >> 23) & 0xff) - 127;
+  return (u & 0x807fffffu) == 0 && e >= -23 && e <= 12;
+}
+
+// two E2M1 codes (one byte, element 2i in the low nibble) -> f16x2
+__device__ __forceinline__ uint32_t e2m1x2_f16x2(uint32_t byte) {
+  uint32_t r;
+  const uint16_t v = (uint16_t)byte;
+  asm("{ .reg .b8 t; cvt.u8.u16 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(r) : "h"(v));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, __half2 s) {
+  __half2 x = *reinterpret_cast<__half2 *>(&a);
+  x = __hmul2(x, s);
+  return *reinterpret_cast<uint32_t *>(&x);
+}
+
+// 32 E2M1 codes (16 bytes) times a power-of-two scale -> 32 f16 (4 x uint4)
+__device__ __forceinline__ void dequant32(const uint4 c, float scale, uint4 (&o)[4]) {
+  const __half2 s2 = __float2half2_rn(scale);
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t h[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) h[b] = hmul2_u32(e2m1x2_f16x2((w[i] >> (8 * b)) & 0xffu), s2);
+    o[i] = make_uint4(h[0], h[1], h[2], h[3]);
+  }
+}
+
+struct Params {
+  Batch b;
+  int hi;              // index heads
+  int qt;              // queries per tile = 256 / hi
+  const uint8_t *q_fp4;
+  const float *q_scale;
+  const float *head_w;
+  const uint8_t *k_fp4;
+  const float *k_scale;
+  const int32_t *cand;
+  int block, max_blocks;
+  float *scores;
+  int64_t ld;
+  int32_t *d_err;
+};
+
+// key row of slot s of run `ri` (or -1 when the slot holds no visible entry):
+// full mode, entry s of the run's request; pool mode, the entry of the
+// query's candidate-block slot.
+__device__ __forceinline__ int64_t slot_row(const Params &P, const Misc *ms, int ri, int64_t s,
+                                            int q) {
+  const RunInfo &ru = ms->runs[ri];
+  if (s >= ru.len) return -1;
+  int64_t j = s;
+  if (P.cand) {
+    j = (int64_t)P.cand[(int64_t)q * P.max_blocks + s / P.block] * P.block + s % P.block;
+    if (j >= ms->n_vis[ru.ql0]) return -1;
+  }
+  return P.b.kv_start[ru.req] + j;
+}
+
+// ---------------------------------------------------------------------------
+__device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms, int q0, int y) {
+  const int ptid = threadIdx.x - kProdWarp0 * 32;
+  const int lane = threadIdx.x & 31;
+  int err = 0;
+  uint32_t it = 0;
+  bool ok = true;
+  for (int ri = 0; ri < ms->nruns && ok; ++ri) {
+    const RunInfo ru = ms->runs[ri];
+    const int q = q0 + ru.ql0;
+    const int64_t nt = (ru.len + kKeyTile - 1) / kKeyTile;
+    for (int64_t kt = (int64_t)y * kTilesPerChunk; kt < nt && kt < (int64_t)(y + 1) * kTilesPerChunk;
+         ++kt, ++it) {
+      const uint32_t st = it % kStages;
+      // 128 keys x 4 groups of 32 elements
+      uint4 codes[(kKeyTile * 4 + kProdThreads - 1) / kProdThreads];
+      float scs[(kKeyTile * 4 + kProdThreads - 1) / kProdThreads];
+#pragma unroll
+      for (int i = 0; i < (kKeyTile * 4 + kProdThreads - 1) / kProdThreads; ++i) {
+        const int item = ptid + i * kProdThreads;
+        codes[i] = make_uint4(0, 0, 0, 0);
+        scs[i] = 0.f;
+        if (item < kKeyTile * 4) {
+          const int row = item >> 2, grp = item & 3;
+          const int64_t g = slot_row(P, ms, ri, kt * kKeyTile + row, q);
+          if (g >= 0) {
+            codes[i] = __ldg(reinterpret_cast<const uint4 *>(P.k_fp4 + g * 64) + grp);
+            scs[i] = __ldg(P.k_scale + g * 4 + grp);
+          }
+        }
+      }
+      if (!(ok = wait_bar(&ms->a_empty[st], ((it / kStages) & 1) ^ 1, ms))) break;
+      uint8_t *A = smem + kOffA + st * kAStage;
+#pragma unroll
+      for (int i = 0; i < (kKeyTile * 4 + kProdThreads - 1) / kProdThreads; ++i) {
+        const int item = ptid + i * kProdThreads;
+        if (item < kKeyTile * 4) {
+          const int row = item >> 2, grp = item & 3;
+          if (scs[i] != 0.f && !mx_scale_ok(scs[i])) err |= CSA2_DERR_SCALE;
+          uint4 o[4];
+          dequant32(codes[i], scs[i], o);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4 *>(A + sw128_offset(row, grp * 32 + c * 8, kABlock)) = o[c];
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ms->a_full[st]);
+    }
+  }
+  err = __reduce_or_sync(0xffffffffu, err);
+  if (lane == 0) raise_err(P.d_err, err);
+}
+
+__device__ void mma_role(const Params &P, uint8_t *smem, Misc *ms, int y) {
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) {
+    const uint32_t tmem = ms->tmem_base;
+    const uint32_t b0 = smem_u32(smem + kOffB);
+    uint32_t it = 0;
+    bool ok = true;
+    for (int ri = 0; ri < ms->nruns && ok; ++ri) {
+      const RunInfo ru = ms->runs[ri];
+      const int64_t nt = (ru.len + kKeyTile - 1) / kKeyTile;
+      uint32_t n = (uint32_t)(ru.nq * P.hi);
+      n = (n + 15u) & ~15u;
+      const uint32_t idesc = make_idesc_f16(128, n, false, false);
+      const uint32_t brow = (uint32_t)(ru.ql0 * P.hi) * 128u;   // byte offset of the run's rows
+      for (int64_t kt = (int64_t)y * kTilesPerChunk;
+           kt < nt && kt < (int64_t)(y + 1) * kTilesPerChunk; ++kt, ++it) {
+        const uint32_t st = it % kStages, db = it & 1;
+        if (!(ok = wait_bar(&ms->a_full[st], (it / kStages) & 1, ms))) break;
+        if (!(ok = wait_bar(&ms->d_empty[db], ((it >> 1) & 1) ^ 1, ms))) break;
+        fence_after_sync();
+        const uint32_t a0 = smem_u32(smem + kOffA + st * kAStage);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a = make_desc_sw128(a0 + (kk >> 2) * kABlock + (kk & 3) * 32, 16, 1024);
+          const uint64_t bq = make_desc_sw128(b0 + (kk >> 2) * kBBlock + brow + (kk & 3) * 32, 16,
+                                              1024);
+          mma_f16(tmem + db * 256, a, bq, idesc, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&ms->a_empty[st]);
+        mma_commit(&ms->d_full[db]);
+      }
+    }
+    mma_commit(&ms->done);
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(&ms->done, 0) && globaltimer() - t0 < kWaitNs) {
+    }
+  }
+  __syncwarp();
+}
+
+template <int HI>
+__device__ void epilogue_role(const Params &P, Misc *ms, int q0, int y) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sp = warp & 3, par = warp >> 2;
+  const uint32_t tmem = ms->tmem_base;
+  const uint32_t lane_addr = (uint32_t)(32 * sp) << 16;
+  constexpr int LW = HI < 32 ? HI : 32;      // columns per TMEM load
+  constexpr int NL = HI / LW;                // loads per query
+  uint32_t it = 0;
+  bool ok = true;
+  for (int ri = 0; ri < ms->nruns && ok; ++ri) {
+    const RunInfo ru = ms->runs[ri];
+    const int64_t nt = (ru.len + kKeyTile - 1) / kKeyTile;
+    for (int64_t kt = (int64_t)y * kTilesPerChunk;
+         kt < nt && kt < (int64_t)(y + 1) * kTilesPerChunk; ++kt, ++it) {
+      const uint32_t db = it & 1;
+      if (!(ok = wait_bar(&ms->d_full[db], (it >> 1) & 1, ms))) break;
+      fence_after_sync();
+      const int64_t s = kt * kKeyTile + 32 * sp + lane;
+      for (int qq = par; qq < ru.nq; qq += 2) {
+        const int ql = ru.ql0 + qq;
+        const int q = q0 + ql;
+        float acc = 0.f;
+#pragma unroll
+        for (int l = 0; l < NL; ++l) {
+          uint32_t v[32];
+          const uint32_t col = db * 256 + (uint32_t)(qq * HI + l * LW);
+          if constexpr (LW == 32) {
+            tmem_ld32x32b_x32(tmem + lane_addr + col, v);
+          } else if constexpr (LW == 16) {
+            tmem_ld32x32b_x16(tmem + lane_addr + col, v);
+          } else {
+            tmem_ld32x32b_x8(tmem + lane_addr + col, v);
+          }
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < LW; ++h)
+            acc = fmaf(ms->w[ql * HI + l * LW + h], fmaxf(__uint_as_float(v[h]), 0.f), acc);
+        }
+        if (s < ms->row_len[ql]) {
+          float outv = acc;
+          if (P.cand) {
+            const int64_t j = (int64_t)P.cand[(int64_t)q * P.max_blocks + s / P.block] * P.block +
+                              s % P.block;
+            if (j >= ms->n_vis[ql]) outv = -INFINITY;
+          }
+          P.scores[(int64_t)q * P.ld + s] = outv;
+        }
+      }
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ms->d_empty[db]);
+    }
+  }
+}
+
+template <int HI>
+__global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Misc *ms = reinterpret_cast<Misc *>(smem + kOffMisc);
+  constexpr int QT = 256 / HI;
+  const int q0 = blockIdx.x * QT;
+  const int y = blockIdx.y;
+  const int warp = threadIdx.x >> 5;
+  int err = 0;
+  // ---- tile geometry (thread 0) -----------------------------------------
+  if (threadIdx.x == 0) {
+    int nr = 0;
+    for (int ql = 0; ql < QT; ++ql) {
+      const int q = q0 + ql;
+      ms->row_len[ql] = 0;
+      ms->n_vis[ql] = 0;
+      if (q >= P.b.num_q) continue;
+      const int r = P.b.q_req[q];
+      int64_t nv = n_visible(P.b.q_pos[q], P.b.ratio);
+      if (nv > P.b.kv_len[r]) {
+        nv = P.b.kv_len[r];
+        if (y == 0) err |= CSA2_DERR_RANGE_CTX;
+      }
+      int64_t len = nv;
+      if (P.cand) {
+        int nb = 0;
+        const int32_t *cb = P.cand + (int64_t)q * P.max_blocks;
+        while (nb < P.max_blocks && cb[nb] >= 0) ++nb;
+        len = (int64_t)nb * P.block;
+      }
+      if (len > P.ld) {
+        len = P.ld;
+        if (y == 0) err |= CSA2_DERR_LD;
+      }
+      ms->row_len[ql] = len;
+      ms->n_vis[ql] = nv;
+      if (!P.cand && nr > 0 && ms->runs[nr - 1].req == r &&
+          ms->runs[nr - 1].ql0 + ms->runs[nr - 1].nq == ql) {
+        RunInfo &ru = ms->runs[nr - 1];
+        ru.nq += 1;
+        if (len > ru.len) ru.len = len;
+      } else {
+        ms->runs[nr].ql0 = ql;
+        ms->runs[nr].nq = 1;
+        ms->runs[nr].req = r;
+        ms->runs[nr].len = len;
+        ++nr;
+      }
+    }
+    ms->nruns = nr;
+    ms->abort = 0;
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&ms->a_full[i], kProdWarps);
+      mbar_init(&ms->a_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ms->d_full[i], 1);
+      mbar_init(&ms->d_empty[i], kEpiWarps);
+    }
+    mbar_init(&ms->done, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  // does this CTA's key chunk hold any work?
+  bool any = false;
+  for (int ri = 0; ri < ms->nruns; ++ri)
+    any |= (ms->runs[ri].len + kKeyTile - 1) / kKeyTile > (int64_t)y * kTilesPerChunk;
+  if (!any) {
+    if (threadIdx.x == 0) raise_err(P.d_err, err);
+    return;
+  }
+  // ---- query operand B: (query, head) rows x 128 f16, and head weights ----
+  uint8_t *B = smem + kOffB;
+  for (int i = threadIdx.x; i < kBRows * 4; i += kThreads) {
+    const int row = i >> 2, grp = i & 3;
+    const int ql = row / HI, h = row % HI;
+    const int q = q0 + ql;
+    uint4 o[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                  make_uint4(0, 0, 0, 0)};
+    if (ql < QT && q < P.b.num_q) {
+      const int64_t base = (int64_t)q * HI + h;
+      const uint4 c = __ldg(reinterpret_cast<const uint4 *>(P.q_fp4 + base * 64) + grp);
+      const float sc = __ldg(P.q_scale + base * 4 + grp);
+      if (!mx_scale_ok(sc) && y == 0) err |= CSA2_DERR_SCALE;
+      dequant32(c, sc, o);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<uint4 *>(B + sw128_offset(row, grp * 32 + c * 8, kBBlock)) = o[c];
+  }
+  for (int i = threadIdx.x; i < QT * HI; i += kThreads) {
+    const int q = q0 + i / HI;
+    ms->w[i] = (q < P.b.num_q) ? (P.head_w ? P.head_w[(int64_t)q * HI + i % HI] : 1.f) : 0.f;
+  }
+  fence_proxy_async_smem();
+  if (warp == kMmaWarp) {
+    tmem_alloc(&ms->tmem_base, 512);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp < kEpiWarps) {
+    epilogue_role<HI>(P, ms, q0, y);
+  } else if (warp == kMmaWarp) {
+    mma_role(P, smem, ms, y);
+  } else {
+    producer_role(P, smem, ms, q0, y);
+  }
+  err = __reduce_or_sync(0xffffffffu, err);
+  if ((threadIdx.x & 31) == 0) raise_err(P.d_err, err);
+  fence_before_sync();
+  __syncthreads();
+  if (ms->abort && threadIdx.x == 0) raise_err(P.d_err, kDerrTimeout);
+  if (warp == kMmaWarp) {
+    fence_after_sync();
+    tmem_dealloc(ms->tmem_base, 512);
+  }
+}
+
+}  // namespace
+
+int index_score_tc(const Batch &b, int n_heads, const uint8_t *q_fp4, const float *q_scale,
+                   const float *head_w, const uint8_t *k_fp4, const float *k_scale,
+                   const int32_t *cand_blocks, int block, int max_blocks, float *scores,
+                   int64_t ld, int32_t *d_err, cudaStream_t st) {
+  if (b.num_q == 0) return CSA2_OK;
+  if (((uintptr_t)q_fp4 | (uintptr_t)k_fp4) & 15u) return CSA2_ERR_UNSUPPORTED;
+  if (((uintptr_t)q_scale | (uintptr_t)k_scale) & 15u) return CSA2_ERR_UNSUPPORTED;
+  Params P;
+  P.b = b;
+  P.hi = n_heads;
+  P.qt = 256 / n_heads;
+  P.q_fp4 = q_fp4;
+  P.q_scale = q_scale;
+  P.head_w = head_w;
+  P.k_fp4 = k_fp4;
+  P.k_scale = k_scale;
+  P.cand = cand_blocks;
+  P.block = block;
+  P.max_blocks = max_blocks;
+  P.scores = scores;
+  P.ld = ld;
+  P.d_err = d_err;
+  int64_t max_len = cand_blocks ? (int64_t)max_blocks * block : ld;
+  if (max_len > ld) max_len = ld;
+  const int64_t chunks = (max_len + kKeyTile * kTilesPerChunk - 1) / (kKeyTile * kTilesPerChunk);
+  if (chunks == 0) return CSA2_OK;
+  if (chunks > 65535) return CSA2_ERR_UNSUPPORTED;
+  const int64_t tiles = (b.num_q + P.qt - 1) / P.qt;
+  dim3 grid((unsigned)tiles, (unsigned)chunks);
+#define CSA2_LAUNCH(H)                                                                     \
+  do {                                                                                     \
+    cudaFuncSetAttribute(index_score_tc_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                         (int)kSmemBytes);                                                 \
+    index_score_tc_kernel<H><<<grid, kThreads, kSmemBytes, st>>>(P);                       \
+  } while (0)
+  switch (n_heads) {
+    case 8: CSA2_LAUNCH(8); break;
+    case 16: CSA2_LAUNCH(16); break;
+    case 32: CSA2_LAUNCH(32); break;
+    case 64: CSA2_LAUNCH(64); break;
+    default: return CSA2_ERR_UNSUPPORTED;
+  }
+#undef CSA2_LAUNCH
+  return launch_status();
+}
+
+}  // namespace csa2

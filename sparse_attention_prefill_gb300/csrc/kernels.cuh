@@ -4,10 +4,10 @@
 
 namespace csa2 {
 
-int index_score_simt(const Batch &b, int n_heads, const uint8_t *q_fp4, const float *q_scale,
-                     const float *head_w, const uint8_t *k_fp4, const float *k_scale,
-                     const int32_t *cand_blocks, int block, int max_blocks, float *scores,
-                     int64_t ld, int32_t *d_err, cudaStream_t st);
+int index_score_tc(const Batch &b, int n_heads, const uint8_t *q_fp4, const float *q_scale,
+                   const float *head_w, const uint8_t *k_fp4, const float *k_scale,
+                   const int32_t *cand_blocks, int block, int max_blocks, float *scores,
+                   int64_t ld, int32_t *d_err, cudaStream_t st);
 
 int topk_launch(const Batch &b, const float *scores, int64_t ld, int k,
                 const int32_t *cand_blocks, int block, int max_blocks, int32_t *idx,
