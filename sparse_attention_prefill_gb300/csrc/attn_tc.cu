@@ -55,9 +55,10 @@ constexpr uint32_t kRBlock = 16384;
 constexpr uint32_t kOffQ = 131072;      // 8 blocks x [64 heads x 128 B]  (64 KB)
 constexpr uint32_t kQBlock = 8192;
 constexpr uint32_t kOffP = 196608;      // [128 rows x 64 heads] f16       (16 KB)
-constexpr uint32_t kOffList = 212992;   // int32 [kMaxSel]                 (8 KB)
-constexpr uint32_t kOffMisc = 221184;
+constexpr uint32_t kOffList = 212992;   // 2 x int32 [kMaxSel]             (16 KB)
+constexpr uint32_t kOffMisc = 229376;
 constexpr uint32_t kSmemBytes = kOffMisc + 2048;
+static_assert(kSmemBytes <= 232448, "shared memory");
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
@@ -70,16 +71,25 @@ constexpr int kDerrTimeout = 128;
 struct Misc {
   uint64_t q_full, q_empty, s_full[2], s_empty[2], p_full, p_empty, o_full, o_empty, done;
   uint64_t r_full[4], r_empty[4];
-  uint64_t sm_grp, pr_grp;  // group syncs of the softmax warps / the producer warps
+  uint64_t sm_grp;          // group sync of the softmax warps
+  uint64_t meta_full[2];
+  int64_t meta[2][4];       // per query (ring of 2): selected rows, window rows, first SWA
+                            // row, pool row of the request's entry 0
   uint32_t tmem_base;
   int abort;
   int votes[2][8];      // softmax warps: "a logit exceeded the reference", by chunk parity
   float m_ref[64];      // reference maximum per head (log2 units)
   float alpha[64];      // rescale factors of the current slow path
   float red[4][64];     // cross-warp reductions
-  int nsel;             // producers: valid selected rows of the current query
 };
 static_assert(sizeof(Misc) <= 2048, "misc region");
+
+// 2^x on the special-function unit (ex2.approx: relative error ~2^-22)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
@@ -131,16 +141,23 @@ __device__ Rows query_rows(const Batch &b, int q, const int32_t *__restrict__ id
   Rows o;
   o.err = 0;
   int64_t cnt = 0;
-  for (int i0 = 0; i0 < k; i0 += 32) {
-    const int i = i0 + lane;
-    int64_t j = -1;
-    if (i < k) j = idx[(int64_t)q * k + i];
-    const bool bad = j >= 0 && (j >= n_vis || j >= kvn);
-    const bool ok = j >= 0 && !bad;
-    if (__any_sync(0xffffffffu, bad)) o.err |= CSA2_DERR_RANGE_IDX;
-    const uint32_t m = __ballot_sync(0xffffffffu, ok);
-    if (list && ok) list[cnt + __popc(m & ((1u << lane) - 1u))] = (int)j;
-    cnt += __popc(m);
+  for (int base = 0; base < k; base += 512) {
+    int32_t jv[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int i = base + u * 32 + lane;
+      jv[u] = i < k ? __ldg(idx + (int64_t)q * k + i) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int64_t j = jv[u];
+      const bool bad = j >= 0 && (j >= n_vis || j >= kvn);
+      const bool ok = j >= 0 && !bad;
+      if (__any_sync(0xffffffffu, bad)) o.err |= CSA2_DERR_RANGE_IDX;
+      const uint32_t m = __ballot_sync(0xffffffffu, ok);
+      if (list && ok) list[cnt + __popc(m & ((1u << lane) - 1u))] = (int)j;
+      cnt += __popc(m);
+    }
   }
   o.nsel = cnt;
   int64_t lo = t - window + 1;
@@ -207,30 +224,36 @@ constexpr int kItemsPerThread = (kItemsPerStep + kProducerThreads - 1) / kProduc
 __device__ __forceinline__ void load_step(const Params &P, const int *list, const Rows &rows,
                                           int64_t kv0, int chunk, int pair, int ptid,
                                           Item (&it)[kItemsPerThread]) {
+  // addresses first (branch-free: rows without data read the first SWA row
+  // and are zeroed afterwards), then every load of the step in one batch
+  const uint8_t *src[kItemsPerThread];
+  const float *sc[kItemsPerThread];
+  bool valid[kItemsPerThread];
 #pragma unroll
   for (int i = 0; i < kItemsPerThread; ++i) {
     const int item = ptid + i * kProducerThreads;
-    it[i].codes = make_uint4(0, 0, 0, 0);
-    it[i].scale = 0.f;
-    if (item < kItemsPerStep) {
-      const int row = item >> 3, seg = item & 7;
-      const int64_t ri = (int64_t)chunk * kRowsPerChunk + row;
-      const int d = pair * 128 + seg * 16;
-      const uint8_t *src = nullptr;
-      const float *sc = nullptr;
-      if (ri < rows.nsel) {
-        const int64_t g = kv0 + list[ri];
-        src = P.kv_fp8 + g * kDim;
-        sc = P.kv_scale + g * (kDim / 32);
-      } else if (ri < rows.nsel + rows.nwin) {
-        const int64_t g = rows.win_first + (ri - rows.nsel);
-        src = P.swa_fp8 + g * kDim;
-        sc = P.swa_scale + g * (kDim / 32);
-      }
-      if (src) {
-        it[i].codes = __ldg(reinterpret_cast<const uint4 *>(src + d));
-        it[i].scale = __ldg(sc + d / 32);
-      }
+    const int row = (item >> 3) & (kRowsPerChunk - 1), seg = item & 7;
+    const int64_t ri = (int64_t)chunk * kRowsPerChunk + row;
+    const int d = pair * 128 + seg * 16;
+    const bool sel = ri < rows.nsel;
+    const bool win = !sel && ri < rows.nsel + rows.nwin;
+    valid[i] = item < kItemsPerStep && (sel || win);
+    const int64_t g = sel ? kv0 + list[sel ? ri : 0] : rows.win_first + (ri - rows.nsel);
+    const uint8_t *base = sel ? P.kv_fp8 : P.swa_fp8;
+    const float *sbase = sel ? P.kv_scale : P.swa_scale;
+    src[i] = valid[i] ? base + g * kDim + d : P.swa_fp8;
+    sc[i] = valid[i] ? sbase + g * (kDim / 32) + d / 32 : P.swa_scale;
+  }
+#pragma unroll
+  for (int i = 0; i < kItemsPerThread; ++i) {
+    it[i].codes = __ldg(reinterpret_cast<const uint4 *>(src[i]));
+    it[i].scale = __ldg(sc[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < kItemsPerThread; ++i) {
+    if (!valid[i]) {
+      it[i].codes = make_uint4(0, 0, 0, 0);
+      it[i].scale = 0.f;
     }
   }
 }
@@ -264,79 +287,82 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms) {
   const int lane = threadIdx.x & 31;
   uint8_t *R = smem + kOffR;
   uint8_t *Qs = smem + kOffQ;
-  int *list = reinterpret_cast<int *>(smem + kOffList);
-  int err = 0;
+  const int *lists = reinterpret_cast<const int *>(smem + kOffList);
   uint32_t g = 0;  // chunks produced by this CTA
-  uint32_t qi = 0, gp = 0;
+  uint32_t qi = 0;
   for (int q = blockIdx.x; q < P.b.num_q; q += gridDim.x, ++qi) {
     // ---- Q of this query (f16, heads zero-padded to 64)
     if (!wait_bar(&ms->q_empty, (qi & 1) ^ 1, ms)) break;
     const __nv_bfloat16 *qg = P.q + (int64_t)q * P.n_heads * kDim;
-#pragma unroll 4
+    // raw bf16 chunks land at their final swizzled place; each thread then
+    // converts exactly the chunks it copied (f16 and bf16 are both 2 bytes)
     for (int it = ptid; it < kHeadsPad * (kDim / 8); it += kProducerThreads) {
       const int h = it / (kDim / 8), d = (it % (kDim / 8)) * 8;
-      uint4 v = make_uint4(0, 0, 0, 0);
+      uint8_t *dst = Qs + sw128_offset(h, d, kQBlock);
       if (h < P.n_heads) {
-        const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(qg + (int64_t)h * kDim + d));
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xffff0000u);
-          __half2 hh = __floats2half2_rn(lo, hi);
-          o[j] = *reinterpret_cast<uint32_t *>(&hh);
-        }
-        v = make_uint4(o[0], o[1], o[2], o[3]);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
+                     "l"(qg + (int64_t)h * kDim + d)
+                     : "memory");
+      } else {
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
       }
-      *reinterpret_cast<uint4 *>(Qs + sw128_offset(h, d, kQBlock)) = v;
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    for (int it = ptid; it < P.n_heads * (kDim / 8); it += kProducerThreads) {
+      const int h = it / (kDim / 8), d = (it % (kDim / 8)) * 8;
+      uint4 *p4 = reinterpret_cast<uint4 *>(Qs + sw128_offset(h, d, kQBlock));
+      const uint4 raw = *p4;
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xffff0000u);
+        __half2 hh = __floats2half2_rn(lo, hi);
+        o[j] = *reinterpret_cast<uint32_t *>(&hh);
+      }
+      *p4 = make_uint4(o[0], o[1], o[2], o[3]);
     }
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&ms->q_full);
     // ---- row list (first producer warp), shared with the other producers
-    Rows rows{0, 0, 0, 0};
-    if (threadIdx.x / 32 == kProducerWarp0) {
-      rows = query_rows(P.b, q, P.idx, P.k, P.win_lo, P.window, list);
-      err |= rows.err;
-      if (lane == 0) ms->nsel = (int)rows.nsel;
-    }
-    if (!group_sync(&ms->pr_grp, gp, ms)) break;
-    {
-      // every producer recomputes the window part (cheap) and reads nsel
-      Rows r2 = query_rows(P.b, q, nullptr, 0, P.win_lo, P.window, nullptr);
-      rows.nwin = r2.nwin;
-      rows.win_first = r2.win_first;
-      rows.nsel = ms->nsel;
-    }
-    const int64_t kv0 = P.b.kv_start[P.b.q_req[q]];
+    // ---- row list and counts of this query (built one query ahead by the
+    // first softmax warp)
+    const uint32_t ms_slot = qi & 1;
+    if (!wait_bar(&ms->meta_full[ms_slot], (qi >> 1) & 1, ms)) break;
+    const int *list = lists + ms_slot * kMaxSel;
+    Rows rows;
+    rows.nsel = ms->meta[ms_slot][0];
+    rows.nwin = ms->meta[ms_slot][1];
+    rows.win_first = ms->meta[ms_slot][2];
+    rows.err = 0;
+    const int64_t kv0 = ms->meta[ms_slot][3];
     const int nch = n_chunks_of(rows.nsel + rows.nwin);
-    // ---- chunks: 4 steps of 128 channels each, loads issued before the wait
-    Item cur[kItemsPerThread], nxt[kItemsPerThread];
-    load_step(P, list, rows, kv0, 0, 0, ptid, cur);
+    // ---- chunks: 4 steps of 128 channels each; the loads of the next two
+    // steps are in flight while a step waits for its buffer and is stored
+    const int nsteps = nch * 4;
+    Item b0[kItemsPerThread], b1[kItemsPerThread], b2[kItemsPerThread];
+    load_step(P, list, rows, kv0, 0, 0, ptid, b0);
+    if (nsteps > 1) load_step(P, list, rows, kv0, 0, 1, ptid, b1);
     bool ok = true;
-    for (int c = 0; c < nch && ok; ++c, ++g) {
-#pragma unroll 1
-      for (int pair = 0; pair < 4; ++pair) {
-        const int nc = pair == 3 ? c + 1 : c, np = (pair + 1) & 3;
-        if (nc < nch) load_step(P, list, rows, kv0, nc, np, ptid, nxt);
-        if (!wait_bar(&ms->r_empty[pair], (g & 1) ^ 1, ms)) {
-          ok = false;
-          break;
-        }
-        store_step(R, pair, ptid, cur);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ms->r_full[pair]);
-#pragma unroll
-        for (int i = 0; i < kItemsPerThread; ++i) cur[i] = nxt[i];
-      }
+    // one step: prefetch step st+2 into `pre`, then store step st from `use`
+    auto step = [&](int st, Item(&use)[kItemsPerThread], Item(&pre)[kItemsPerThread]) -> bool {
+      const int c = st >> 2, pair = st & 3;
+      if (st + 2 < nsteps) load_step(P, list, rows, kv0, (st + 2) >> 2, (st + 2) & 3, ptid, pre);
+      if (!wait_bar(&ms->r_empty[pair], ((g + c) & 1) ^ 1, ms)) return false;
+      store_step(R, pair, ptid, use);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ms->r_full[pair]);
+      return true;
+    };
+    for (int st = 0; st < nsteps && ok; st += 3) {
+      ok = step(st, b0, b2);
+      if (ok && st + 1 < nsteps) ok = step(st + 1, b1, b0);
+      if (ok && st + 2 < nsteps) ok = step(st + 2, b2, b1);
     }
+    g += nch;
     if (!ok) break;
-    if (!group_sync(&ms->pr_grp, gp, ms)) break;  // the list is rebuilt for the next query
-  }
-  if (threadIdx.x / 32 == kProducerWarp0) {
-    err = __reduce_or_sync(0xffffffffu, err);
-    if (lane == 0) raise_err(P.d_err, err);
   }
 }
 
@@ -353,10 +379,11 @@ __device__ void mma_role(const Params &P, uint8_t *smem, Misc *ms) {
   const uint32_t id_o = make_idesc_f16(128, kHeadsPad, true, true);
   uint32_t g = 0, qi = 0;
   int ok = 1;
-  for (int q = blockIdx.x; q < P.b.num_q; q += gridDim.x, ++qi) {
-    const Rows rows = query_rows(P.b, q, P.idx, P.k, P.win_lo, P.window, nullptr);
-    const int nch = n_chunks_of(rows.nsel + rows.nwin);
-    if (lane == 0) {
+  for (int q = blockIdx.x; q < P.b.num_q && lane == 0; q += gridDim.x, ++qi) {
+    {
+      const uint32_t slot = qi & 1;
+      if (!(ok = wait_bar(&ms->meta_full[slot], (qi >> 1) & 1, ms))) break;
+      const int nch = n_chunks_of(ms->meta[slot][0] + ms->meta[slot][1]);
       for (int c = 0; c < nch && ok; ++c, ++g) {
         const uint32_t sb = g & 1;
         const uint32_t s_tmem = tmem + kColS + sb * 64;
@@ -396,7 +423,6 @@ __device__ void mma_role(const Params &P, uint8_t *smem, Misc *ms) {
         if (c == nch - 1) mma_commit(&ms->o_full);
       }
     }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) break;
   }
   // drain: every MMA issued so far has completed once `done` flips (bounded
@@ -425,12 +451,35 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
   float lsum[32];
   uint32_t g = 0, qi = 0, gp = 0;
   bool ok = true;
+  int err = 0;
+  int *lists = reinterpret_cast<int *>(smem + kOffList);
+  // Row lists and counts are built by warp 0 one query ahead of their use.
+  // Slot (qi+1)&1 was last read for query qi-1, whose chunks have all been
+  // produced and consumed before this role reaches query qi.
+  auto publish = [&](int qn, uint32_t qin) {
+    if (warp != 0 || qn >= P.b.num_q) return;
+    const uint32_t slot = qin & 1;
+    const Rows r1 = query_rows(P.b, qn, P.idx, P.k, P.win_lo, P.window, lists + slot * kMaxSel);
+    err |= r1.err;
+    const int64_t kv0 = P.b.kv_start[P.b.q_req[qn]];
+    __syncwarp();
+    if (lane == 0) {
+      ms->meta[slot][0] = r1.nsel;
+      ms->meta[slot][1] = r1.nwin;
+      ms->meta[slot][2] = r1.win_first;
+      ms->meta[slot][3] = kv0;
+      mbar_arrive(&ms->meta_full[slot]);
+    }
+  };
+  publish(blockIdx.x, 0);
   if (stid < 64) ms->m_ref[stid] = NEG_INF;
   ok = group_sync(&ms->sm_grp, gp, ms);
   for (int q = blockIdx.x; q < P.b.num_q && ok; q += gridDim.x, ++qi) {
-    const Rows rows = query_rows(P.b, q, P.idx, P.k, P.win_lo, P.window, nullptr);
-    const int64_t nrows = rows.nsel + rows.nwin;
+    const uint32_t slot = qi & 1;
+    if (!(ok = wait_bar(&ms->meta_full[slot], (qi >> 1) & 1, ms))) break;
+    const int64_t nrows = ms->meta[slot][0] + ms->meta[slot][1];
     const int nch = n_chunks_of(nrows);
+    publish(q + gridDim.x, qi + 1);
 #pragma unroll
     for (int j = 0; j < 32; ++j) lsum[j] = 0.f;
     for (int c = 0; c < nch; ++c, ++g) {
@@ -462,23 +511,17 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
 #pragma unroll
       for (int w = 0; w < kSoftmaxWarps; ++w) slow |= ms->votes[vb][w] != 0;
       if (slow) {
-        // per-head maximum over the chunk's 128 rows: transposed butterfly in
-        // the warp (lane j ends with head 32*hh + j), then across the 4 warps
-        float y[32];
+        // per-head maximum over the warp's 32 rows (butterfly per head), then
+        // across the 4 warps of this head half
+        float mine = NEG_INF;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) y[j] = x[j];
+        for (int j = 0; j < 32; ++j) {
+          float mj = x[j];
 #pragma unroll
-        for (int w = 16; w >= 1; w >>= 1) {
-          const bool upper = (lane & w) != 0;
-#pragma unroll
-          for (int j = 0; j < w; ++j) {
-            const float send = upper ? y[j] : y[j + w];
-            const float keep = upper ? y[j + w] : y[j];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, w);
-            y[j] = fmaxf(keep, recv);
-          }
+          for (int w = 16; w >= 1; w >>= 1) mj = fmaxf(mj, __shfl_xor_sync(0xffffffffu, mj, w));
+          if (lane == j) mine = mj;
         }
-        ms->red[sp][32 * hh + lane] = y[0];
+        ms->red[sp][32 * hh + lane] = mine;
         if (!(ok = group_sync(&ms->sm_grp, gp, ms))) break;
         if (stid < 64) {
           const float old = ms->m_ref[stid];
@@ -498,15 +541,17 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
       if (!ok) break;
       fence_after_sync();
       if (slow && c > 0) {
-        for (int t = 0; t < 4; ++t) {
+#pragma unroll 1
+        for (int t = 0; t < 8; ++t) {   // 4 tiles x 2 halves of this warp's 32 heads
           uint32_t o[32];
-          const uint32_t a = tmem + lane_addr + kColO + t * 64 + 32 * hh;
-          tmem_ld32x32b_x32(a, o);
+          const int hb = 32 * hh + 16 * (t & 1);
+          const uint32_t a = tmem + lane_addr + kColO + (t >> 1) * 64 + 16 * (t & 1) + 32 * hh;
+          tmem_ld32x32b_x16(a, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            o[j] = __float_as_uint(__uint_as_float(o[j]) * ms->alpha[32 * hh + j]);
-          tmem_st32x32b_x32(a, o);
+          for (int j = 0; j < 16; ++j)
+            o[j] = __float_as_uint(__uint_as_float(o[j]) * ms->alpha[hb + j]);
+          tmem_st32x32b_x16(a, o);
         }
         tmem_wait_st();
       }
@@ -514,8 +559,8 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
         const float m0 = ms->m_ref[32 * hh + j], m1 = ms->m_ref[32 * hh + j + 1];
-        const float p0 = exp2f(x[j] - (m0 == NEG_INF ? 0.f : m0));
-        const float p1 = exp2f(x[j + 1] - (m1 == NEG_INF ? 0.f : m1));
+        const float p0 = ex2(x[j] - (m0 == NEG_INF ? 0.f : m0));
+        const float p1 = ex2(x[j + 1] - (m1 == NEG_INF ? 0.f : m1));
         lsum[j] += p0;
         lsum[j + 1] += p1;
         __half2 h2 = __floats2half2_rn(p0, p1);
@@ -533,17 +578,15 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
     }
     if (!ok) break;
     // ---- epilogue: row sums, normalisation, bf16 output, lse
+    float lmine = 0.f;
 #pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) {
-      const bool upper = (lane & w) != 0;
+    for (int j = 0; j < 32; ++j) {
+      float lj = lsum[j];
 #pragma unroll
-      for (int j = 0; j < w; ++j) {
-        const float send = upper ? lsum[j] : lsum[j + w];
-        const float keep = upper ? lsum[j + w] : lsum[j];
-        lsum[j] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-      }
+      for (int w = 16; w >= 1; w >>= 1) lj += __shfl_xor_sync(0xffffffffu, lj, w);
+      if (lane == j) lmine = lj;
     }
-    ms->red[sp][32 * hh + lane] = lsum[0];
+    ms->red[sp][32 * hh + lane] = lmine;
     if (!(ok = group_sync(&ms->sm_grp, gp, ms))) break;
     if (stid < 64) {
       float l = (ms->red[0][stid] + ms->red[1][stid]) + (ms->red[2][stid] + ms->red[3][stid]);
@@ -577,6 +620,10 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
     __syncwarp();
     if (lane == 0) mbar_arrive(&ms->o_empty);
   }
+  if (warp == 0) {
+    err = __reduce_or_sync(0xffffffffu, err);
+    if (lane == 0) raise_err(P.d_err, err);
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(Params P) {
@@ -600,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(Params P) {
       mbar_init(&ms->r_empty[i], 1);
     }
     mbar_init(&ms->sm_grp, kSoftmaxWarps);
-    mbar_init(&ms->pr_grp, kProducerWarps);
+    for (int i = 0; i < 2; ++i) mbar_init(&ms->meta_full[i], 1);
     ms->abort = 0;
     mbar_fence_init();
   }
@@ -649,6 +696,8 @@ int attn_tc(const Batch &b, int n_heads, const __nv_bfloat16 *q, const uint8_t *
             cudaStream_t st) {
   if (b.num_q == 0) return CSA2_OK;
   if (n_heads > kHeadsPad || k > kMaxSel) return CSA2_ERR_UNSUPPORTED;
+  // 16-byte vector loads and asynchronous copies need 16-byte aligned rows
+  if (((uintptr_t)q | (uintptr_t)kv_fp8 | (uintptr_t)swa_fp8) & 15u) return CSA2_ERR_UNSUPPORTED;
   Params P;
   P.b = b;
   P.n_heads = n_heads;

@@ -19,10 +19,14 @@
 // Work unit (one CTA): a tile of 256/Hi consecutive query rows and a chunk of
 // 16 key tiles (2048 keys or pool slots).  Rows of the tile that belong to the
 // same request share key tiles ("runs", full mode); in pool mode every query
-// has its own slot list and is its own run.  Roles (12 warps):
+// has its own slot list and is its own run, except that identity pools
+// (blocks 0, 1, ..., nb-1: nothing excluded, the case when every reachable
+// position fits the pool budget) map slot s to entry s and merge like full
+// mode.  Roles (13 warps):
 //   warps 0-7   epilogue (warp w: TMEM lanes 32*(w%4).., queries of parity w/4)
 //   warp 8      TMEM allocation; lane 0 issues the MMAs
-//   warps 9-11  producers: key gather + E2M1 -> f16 into a 4-stage ring
+//   warps 9-12  producers: key gather + E2M1 -> f16 into a 4-stage ring, one
+//               key tile of loads in flight ahead of the ring
 // Waits are time-bounded (CSA2_DERR_TIMEOUT on expiry).
 #include "common.cuh"
 #include "kernels.cuh"
@@ -39,8 +43,8 @@ constexpr int kStages = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kMmaWarp = 8;
 constexpr int kProdWarp0 = 9;
-constexpr int kProdWarps = 3;
-constexpr int kWarps = 12;
+constexpr int kProdWarps = 4;
+constexpr int kWarps = 13;
 constexpr int kThreads = kWarps * 32;
 constexpr int kProdThreads = kProdWarps * 32;
 constexpr int kBRows = 256 + 16;       // (query, head) rows + padding for N rounding
@@ -59,7 +63,9 @@ constexpr int kMaxQT = 32;
 
 struct RunInfo {
   int ql0, nq, req;
+  int gather;   // 1: slots map through the query's candidate blocks
   int64_t len;  // longest row of the run
+  int64_t lim;  // entries below lim hold keys (slots past it are empty)
 };
 
 struct Misc {
@@ -70,6 +76,8 @@ struct Misc {
   RunInfo runs[kMaxQT];
   int64_t row_len[kMaxQT];   // per query of the tile (0 past the batch)
   int64_t n_vis[kMaxQT];
+  int nb[kMaxQT];            // pool mode: candidate blocks per query
+  int ident[kMaxQT];         // pool mode: blocks are 0..nb-1
   float w[256];              // head weights of the tile
 };
 static_assert(sizeof(Misc) <= 4096, "misc");
@@ -150,7 +158,8 @@ __device__ __forceinline__ int64_t slot_row(const Params &P, const Misc *ms, int
   const RunInfo &ru = ms->runs[ri];
   if (s >= ru.len) return -1;
   int64_t j = s;
-  if (P.cand) {
+  if (!ru.gather && s >= ru.lim) return -1;
+  if (ru.gather) {
     j = (int64_t)P.cand[(int64_t)q * P.max_blocks + s / P.block] * P.block + s % P.block;
     if (j >= ms->n_vis[ru.ql0]) return -1;
   }
@@ -158,55 +167,86 @@ __device__ __forceinline__ int64_t slot_row(const Params &P, const Misc *ms, int
 }
 
 // ---------------------------------------------------------------------------
+// producers: the (run, key tile) sequence of this CTA; the loads of tile i+1
+// are issued before tile i is converted and stored.
+// ---------------------------------------------------------------------------
+constexpr int kProdItems = (kKeyTile * 4 + kProdThreads - 1) / kProdThreads;
+
+struct KeyLoad {
+  uint4 codes[kProdItems];
+  float sc[kProdItems];
+};
+
+__device__ __forceinline__ void load_tile(const Params &P, const Misc *ms, int ri, int64_t kt,
+                                          int q, int ptid, KeyLoad &L) {
+#pragma unroll
+  for (int i = 0; i < kProdItems; ++i) {
+    const int item = ptid + i * kProdThreads;
+    L.codes[i] = make_uint4(0, 0, 0, 0);
+    L.sc[i] = 0.f;
+    if (item < kKeyTile * 4) {
+      const int row = item >> 2, grp = item & 3;
+      const int64_t g = slot_row(P, ms, ri, kt * kKeyTile + row, q);
+      if (g >= 0) {
+        L.codes[i] = __ldg(reinterpret_cast<const uint4 *>(P.k_fp4 + g * 64) + grp);
+        L.sc[i] = __ldg(P.k_scale + g * 4 + grp);
+      }
+    }
+  }
+}
+
+// next (run, tile) after (ri, kt) within key chunk y; false when none is left
+__device__ __forceinline__ bool next_item(const Misc *ms, int y, int &ri, int64_t &kt) {
+  ++kt;
+  while (ri < ms->nruns) {
+    const int64_t nt = (ms->runs[ri].len + kKeyTile - 1) / kKeyTile;
+    const int64_t hi = min(nt, (int64_t)(y + 1) * kTilesPerChunk);
+    if (kt < hi) return true;
+    ++ri;
+    kt = (int64_t)y * kTilesPerChunk;
+  }
+  return false;
+}
+
 __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms, int q0, int y) {
   const int ptid = threadIdx.x - kProdWarp0 * 32;
   const int lane = threadIdx.x & 31;
   int err = 0;
   uint32_t it = 0;
-  bool ok = true;
-  for (int ri = 0; ri < ms->nruns && ok; ++ri) {
-    const RunInfo ru = ms->runs[ri];
-    const int q = q0 + ru.ql0;
-    const int64_t nt = (ru.len + kKeyTile - 1) / kKeyTile;
-    for (int64_t kt = (int64_t)y * kTilesPerChunk; kt < nt && kt < (int64_t)(y + 1) * kTilesPerChunk;
-         ++kt, ++it) {
-      const uint32_t st = it % kStages;
-      // 128 keys x 4 groups of 32 elements
-      uint4 codes[(kKeyTile * 4 + kProdThreads - 1) / kProdThreads];
-      float scs[(kKeyTile * 4 + kProdThreads - 1) / kProdThreads];
+  int ri = 0;
+  int64_t kt = (int64_t)y * kTilesPerChunk - 1;
+  if (!next_item(ms, y, ri, kt)) return;
+  KeyLoad cur, nxt;
+  load_tile(P, ms, ri, kt, q0 + ms->runs[ri].ql0, ptid, cur);
+  bool more = true;
+  while (more) {
+    int ri2 = ri;
+    int64_t kt2 = kt;
+    more = next_item(ms, y, ri2, kt2);
+    if (more) load_tile(P, ms, ri2, kt2, q0 + ms->runs[ri2].ql0, ptid, nxt);
+    const uint32_t st = it % kStages;
+    if (!wait_bar(&ms->a_empty[st], ((it / kStages) & 1) ^ 1, ms)) break;
+    uint8_t *A = smem + kOffA + st * kAStage;
 #pragma unroll
-      for (int i = 0; i < (kKeyTile * 4 + kProdThreads - 1) / kProdThreads; ++i) {
-        const int item = ptid + i * kProdThreads;
-        codes[i] = make_uint4(0, 0, 0, 0);
-        scs[i] = 0.f;
-        if (item < kKeyTile * 4) {
-          const int row = item >> 2, grp = item & 3;
-          const int64_t g = slot_row(P, ms, ri, kt * kKeyTile + row, q);
-          if (g >= 0) {
-            codes[i] = __ldg(reinterpret_cast<const uint4 *>(P.k_fp4 + g * 64) + grp);
-            scs[i] = __ldg(P.k_scale + g * 4 + grp);
-          }
-        }
+    for (int i = 0; i < kProdItems; ++i) {
+      const int item = ptid + i * kProdThreads;
+      if (item < kKeyTile * 4) {
+        const int row = item >> 2, grp = item & 3;
+        if (cur.sc[i] != 0.f && !mx_scale_ok(cur.sc[i])) err |= CSA2_DERR_SCALE;
+        uint4 o[4];
+        dequant32(cur.codes[i], cur.sc[i], o);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4 *>(A + sw128_offset(row, grp * 32 + c * 8, kABlock)) = o[c];
       }
-      if (!(ok = wait_bar(&ms->a_empty[st], ((it / kStages) & 1) ^ 1, ms))) break;
-      uint8_t *A = smem + kOffA + st * kAStage;
-#pragma unroll
-      for (int i = 0; i < (kKeyTile * 4 + kProdThreads - 1) / kProdThreads; ++i) {
-        const int item = ptid + i * kProdThreads;
-        if (item < kKeyTile * 4) {
-          const int row = item >> 2, grp = item & 3;
-          if (scs[i] != 0.f && !mx_scale_ok(scs[i])) err |= CSA2_DERR_SCALE;
-          uint4 o[4];
-          dequant32(codes[i], scs[i], o);
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4 *>(A + sw128_offset(row, grp * 32 + c * 8, kABlock)) = o[c];
-        }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ms->a_full[st]);
     }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ms->a_full[st]);
+    ++it;
+    ri = ri2;
+    kt = kt2;
+    cur = nxt;
   }
   err = __reduce_or_sync(0xffffffffu, err);
   if (lane == 0) raise_err(P.d_err, err);
@@ -294,8 +334,10 @@ __device__ void epilogue_role(const Params &P, Misc *ms, int q0, int y) {
         if (s < ms->row_len[ql]) {
           float outv = acc;
           if (P.cand) {
-            const int64_t j = (int64_t)P.cand[(int64_t)q * P.max_blocks + s / P.block] * P.block +
-                              s % P.block;
+            const int64_t j =
+                ru.gather ? (int64_t)P.cand[(int64_t)q * P.max_blocks + s / P.block] * P.block +
+                                s % P.block
+                          : s;
             if (j >= ms->n_vis[ql]) outv = -INFINITY;
           }
           P.scores[(int64_t)q * P.ld + s] = outv;
@@ -317,47 +359,16 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
   const int y = blockIdx.y;
   const int warp = threadIdx.x >> 5;
   int err = 0;
-  // ---- tile geometry (thread 0) -----------------------------------------
+  // ---- tile geometry -------------------------------------------------------
+  // per query: visible entries and, in pool mode, the number of candidate
+  // blocks (first -1) and whether the pool is the identity 0..nb-1 (blocks
+  // are strictly ascending, so that holds iff block nb-1 is nb-1)
+  if (threadIdx.x < QT) {
+    ms->nb[threadIdx.x] = P.max_blocks;
+    ms->row_len[threadIdx.x] = 0;
+    ms->n_vis[threadIdx.x] = 0;
+  }
   if (threadIdx.x == 0) {
-    int nr = 0;
-    for (int ql = 0; ql < QT; ++ql) {
-      const int q = q0 + ql;
-      ms->row_len[ql] = 0;
-      ms->n_vis[ql] = 0;
-      if (q >= P.b.num_q) continue;
-      const int r = P.b.q_req[q];
-      int64_t nv = n_visible(P.b.q_pos[q], P.b.ratio);
-      if (nv > P.b.kv_len[r]) {
-        nv = P.b.kv_len[r];
-        if (y == 0) err |= CSA2_DERR_RANGE_CTX;
-      }
-      int64_t len = nv;
-      if (P.cand) {
-        int nb = 0;
-        const int32_t *cb = P.cand + (int64_t)q * P.max_blocks;
-        while (nb < P.max_blocks && cb[nb] >= 0) ++nb;
-        len = (int64_t)nb * P.block;
-      }
-      if (len > P.ld) {
-        len = P.ld;
-        if (y == 0) err |= CSA2_DERR_LD;
-      }
-      ms->row_len[ql] = len;
-      ms->n_vis[ql] = nv;
-      if (!P.cand && nr > 0 && ms->runs[nr - 1].req == r &&
-          ms->runs[nr - 1].ql0 + ms->runs[nr - 1].nq == ql) {
-        RunInfo &ru = ms->runs[nr - 1];
-        ru.nq += 1;
-        if (len > ru.len) ru.len = len;
-      } else {
-        ms->runs[nr].ql0 = ql;
-        ms->runs[nr].nq = 1;
-        ms->runs[nr].req = r;
-        ms->runs[nr].len = len;
-        ++nr;
-      }
-    }
-    ms->nruns = nr;
     ms->abort = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&ms->a_full[i], kProdWarps);
@@ -371,12 +382,74 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
     mbar_fence_init();
   }
   __syncthreads();
+  if (P.cand) {
+    const int total = QT * P.max_blocks;
+    for (int i = threadIdx.x; i < total; i += kThreads) {
+      const int ql = i / P.max_blocks, bi = i % P.max_blocks;
+      const int q = q0 + ql;
+      if (q < P.b.num_q && P.cand[(int64_t)q * P.max_blocks + bi] < 0) atomicMin(&ms->nb[ql], bi);
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x < QT) {
+    const int ql = threadIdx.x, q = q0 + ql;
+    if (q < P.b.num_q) {
+      const int r = P.b.q_req[q];
+      int64_t nv = n_visible(P.b.q_pos[q], P.b.ratio);
+      if (nv > P.b.kv_len[r]) {
+        nv = P.b.kv_len[r];
+        if (y == 0) err |= CSA2_DERR_RANGE_CTX;
+      }
+      int64_t len = nv;
+      int ident = 1;
+      if (P.cand) {
+        const int nb = ms->nb[ql];
+        len = (int64_t)nb * P.block;
+        ident = nb == 0 || P.cand[(int64_t)q * P.max_blocks + nb - 1] == nb - 1;
+      }
+      if (len > P.ld) {
+        len = P.ld;
+        if (y == 0) err |= CSA2_DERR_LD;
+      }
+      ms->row_len[ql] = len;
+      ms->n_vis[ql] = nv;
+      ms->ident[ql] = ident;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int nr = 0;
+    for (int ql = 0; ql < QT; ++ql) {
+      const int q = q0 + ql;
+      if (q >= P.b.num_q) break;
+      const int r = P.b.q_req[q];
+      const int gather = P.cand && !ms->ident[ql];
+      const int64_t len = ms->row_len[ql];
+      const int64_t lim = len < ms->n_vis[ql] ? len : ms->n_vis[ql];
+      if (!gather && nr > 0 && !ms->runs[nr - 1].gather && ms->runs[nr - 1].req == r) {
+        RunInfo &ru = ms->runs[nr - 1];
+        ru.nq += 1;
+        if (len > ru.len) ru.len = len;
+        if (lim > ru.lim) ru.lim = lim;
+      } else {
+        ms->runs[nr].ql0 = ql;
+        ms->runs[nr].nq = 1;
+        ms->runs[nr].req = r;
+        ms->runs[nr].gather = gather;
+        ms->runs[nr].len = len;
+        ms->runs[nr].lim = lim;
+        ++nr;
+      }
+    }
+    ms->nruns = nr;
+  }
+  __syncthreads();
   // does this CTA's key chunk hold any work?
   bool any = false;
   for (int ri = 0; ri < ms->nruns; ++ri)
     any |= (ms->runs[ri].len + kKeyTile - 1) / kKeyTile > (int64_t)y * kTilesPerChunk;
   if (!any) {
-    if (threadIdx.x == 0) raise_err(P.d_err, err);
+    raise_err(P.d_err, err);
     return;
   }
   // ---- query operand B: (query, head) rows x 128 f16, and head weights ----
