@@ -228,7 +228,6 @@ __device__ __forceinline__ void load_step(const Params &P, const int *list, cons
   // and are zeroed afterwards), then every load of the step in one batch
   const uint8_t *src[kItemsPerThread];
   const float *sc[kItemsPerThread];
-  bool valid[kItemsPerThread];
 #pragma unroll
   for (int i = 0; i < kItemsPerThread; ++i) {
     const int item = ptid + i * kProducerThreads;
@@ -237,47 +236,49 @@ __device__ __forceinline__ void load_step(const Params &P, const int *list, cons
     const int d = pair * 128 + seg * 16;
     const bool sel = ri < rows.nsel;
     const bool win = !sel && ri < rows.nsel + rows.nwin;
-    valid[i] = item < kItemsPerStep && (sel || win);
+    const bool valid = item < kItemsPerStep && (sel || win);
     const int64_t g = sel ? kv0 + list[sel ? ri : 0] : rows.win_first + (ri - rows.nsel);
     const uint8_t *base = sel ? P.kv_fp8 : P.swa_fp8;
     const float *sbase = sel ? P.kv_scale : P.swa_scale;
-    src[i] = valid[i] ? base + g * kDim + d : P.swa_fp8;
-    sc[i] = valid[i] ? sbase + g * (kDim / 32) + d / 32 : P.swa_scale;
+    src[i] = valid ? base + g * kDim + d : P.swa_fp8;
+    sc[i] = valid ? sbase + g * (kDim / 32) + d / 32 : P.swa_scale;
   }
+  // no use of the loaded values here: the mask is applied when the step is
+  // stored, so the loads stay in flight while earlier steps are written
 #pragma unroll
   for (int i = 0; i < kItemsPerThread; ++i) {
     it[i].codes = __ldg(reinterpret_cast<const uint4 *>(src[i]));
     it[i].scale = __ldg(sc[i]);
   }
-#pragma unroll
-  for (int i = 0; i < kItemsPerThread; ++i) {
-    if (!valid[i]) {
-      it[i].codes = make_uint4(0, 0, 0, 0);
-      it[i].scale = 0.f;
-    }
-  }
 }
 
-__device__ __forceinline__ void store_step(uint8_t *R, int pair, int ptid,
-                                           const Item (&it)[kItemsPerThread]) {
+__device__ __forceinline__ void store_step(uint8_t *R, int pair, int ptid, int64_t ri0,
+                                           int64_t nrows, const Item (&it)[kItemsPerThread]) {
 #pragma unroll
   for (int i = 0; i < kItemsPerThread; ++i) {
     const int item = ptid + i * kProducerThreads;
     if (item < kItemsPerStep) {
       const int row = item >> 3, seg = item & 7;
       const int d = pair * 128 + seg * 16;
-      const __half2 s2 = __float2half2_rn(it[i].scale);
-      const uint32_t w[4] = {it[i].codes.x, it[i].codes.y, it[i].codes.z, it[i].codes.w};
+      const bool valid = ri0 + row < nrows;
+      const __half2 s2 = __float2half2_rn(valid ? it[i].scale : 0.f);
+      const uint32_t w[4] = {valid ? it[i].codes.x : 0u, valid ? it[i].codes.y : 0u,
+                             valid ? it[i].codes.z : 0u, valid ? it[i].codes.w : 0u};
       uint32_t h[8];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         h[2 * j] = hmul2_u32(e4m3x2_f16x2(w[j] & 0xffffu), s2);
         h[2 * j + 1] = hmul2_u32(e4m3x2_f16x2(w[j] >> 16), s2);
       }
-      *reinterpret_cast<uint4 *>(R + sw128_offset(row, d, kRBlock)) =
-          make_uint4(h[0], h[1], h[2], h[3]);
-      *reinterpret_cast<uint4 *>(R + sw128_offset(row, d + 8, kRBlock)) =
-          make_uint4(h[4], h[5], h[6], h[7]);
+      // the 8 threads of a store phase cover one row's 8 segments; segments
+      // 0-3 and 4-7 fall in two column blocks whose 16-byte chunks share banks,
+      // so the second block writes its halves in the opposite order: every
+      // phase then touches 8 distinct chunk positions (no bank conflict)
+      const uint4 lo = make_uint4(h[0], h[1], h[2], h[3]);
+      const uint4 hi = make_uint4(h[4], h[5], h[6], h[7]);
+      const bool swap = (seg & 4) != 0;
+      *reinterpret_cast<uint4 *>(R + sw128_offset(row, swap ? d + 8 : d, kRBlock)) = swap ? hi : lo;
+      *reinterpret_cast<uint4 *>(R + sw128_offset(row, swap ? d : d + 8, kRBlock)) = swap ? lo : hi;
     }
   }
 }
@@ -350,7 +351,7 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms) {
       const int c = st >> 2, pair = st & 3;
       if (st + 2 < nsteps) load_step(P, list, rows, kv0, (st + 2) >> 2, (st + 2) & 3, ptid, pre);
       if (!wait_bar(&ms->r_empty[pair], ((g + c) & 1) ^ 1, ms)) return false;
-      store_step(R, pair, ptid, use);
+      store_step(R, pair, ptid, (int64_t)c * kRowsPerChunk, rows.nsel + rows.nwin, use);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ms->r_full[pair]);

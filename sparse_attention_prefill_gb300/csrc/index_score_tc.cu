@@ -216,25 +216,27 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
   int ri = 0;
   int64_t kt = (int64_t)y * kTilesPerChunk - 1;
   if (!next_item(ms, y, ri, kt)) return;
-  KeyLoad cur, nxt;
-  load_tile(P, ms, ri, kt, q0 + ms->runs[ri].ql0, ptid, cur);
+  KeyLoad ka, kb;
+  load_tile(P, ms, ri, kt, q0 + ms->runs[ri].ql0, ptid, ka);
   bool more = true;
-  while (more) {
+  // store the tile held in `use` after issuing the loads of the next tile
+  // into `pre` (two fixed buffers: no register copy waits on pending loads)
+  auto step = [&](KeyLoad &use, KeyLoad &pre) -> bool {
     int ri2 = ri;
     int64_t kt2 = kt;
     more = next_item(ms, y, ri2, kt2);
-    if (more) load_tile(P, ms, ri2, kt2, q0 + ms->runs[ri2].ql0, ptid, nxt);
+    if (more) load_tile(P, ms, ri2, kt2, q0 + ms->runs[ri2].ql0, ptid, pre);
     const uint32_t st = it % kStages;
-    if (!wait_bar(&ms->a_empty[st], ((it / kStages) & 1) ^ 1, ms)) break;
+    if (!wait_bar(&ms->a_empty[st], ((it / kStages) & 1) ^ 1, ms)) return false;
     uint8_t *A = smem + kOffA + st * kAStage;
 #pragma unroll
     for (int i = 0; i < kProdItems; ++i) {
       const int item = ptid + i * kProdThreads;
       if (item < kKeyTile * 4) {
         const int row = item >> 2, grp = item & 3;
-        if (cur.sc[i] != 0.f && !mx_scale_ok(cur.sc[i])) err |= CSA2_DERR_SCALE;
+        if (use.sc[i] != 0.f && !mx_scale_ok(use.sc[i])) err |= CSA2_DERR_SCALE;
         uint4 o[4];
-        dequant32(cur.codes[i], cur.sc[i], o);
+        dequant32(use.codes[i], use.sc[i], o);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           *reinterpret_cast<uint4 *>(A + sw128_offset(row, grp * 32 + c * 8, kABlock)) = o[c];
@@ -246,7 +248,11 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
     ++it;
     ri = ri2;
     kt = kt2;
-    cur = nxt;
+    return true;
+  };
+  while (true) {
+    if (!step(ka, kb) || !more) break;
+    if (!step(kb, ka) || !more) break;
   }
   err = __reduce_or_sync(0xffffffffu, err);
   if (lane == 0) raise_err(P.d_err, err);
