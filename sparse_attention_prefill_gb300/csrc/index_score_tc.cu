@@ -366,11 +366,23 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
   const int warp = threadIdx.x >> 5;
   int err = 0;
   // ---- tile geometry -------------------------------------------------------
-  // per query: visible entries and, in pool mode, the number of candidate
-  // blocks (first -1) and whether the pool is the identity 0..nb-1 (blocks
-  // are strictly ascending, so that holds iff block nb-1 is nb-1)
+  // per query: visible entries and the row length seen by this key chunk.  In
+  // pool mode only the candidate blocks overlapping this chunk's slots are
+  // scanned: the first -1 among them ends the row (blocks are -1 padded at
+  // the end), and the slots of the chunk map through an identity pool iff the
+  // last present block of the range is its own index (blocks are strictly
+  // ascending, so block i >= i, with equality all the way down)
+  const int64_t s_lo = (int64_t)y * kKeyTile * kTilesPerChunk;
+  const int64_t s_hi = s_lo + (int64_t)kKeyTile * kTilesPerChunk;
+  int b_lo = 0, b_hi = 0;
+  if (P.cand) {
+    b_lo = (int)(s_lo / P.block);
+    const int64_t bh = (s_hi + P.block - 1) / P.block;
+    b_hi = (int)(bh < P.max_blocks ? bh : P.max_blocks);
+    if (b_lo > b_hi) b_lo = b_hi;
+  }
   if (threadIdx.x < QT) {
-    ms->nb[threadIdx.x] = P.max_blocks;
+    ms->nb[threadIdx.x] = b_hi;
     ms->row_len[threadIdx.x] = 0;
     ms->n_vis[threadIdx.x] = 0;
   }
@@ -389,9 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
   }
   __syncthreads();
   if (P.cand) {
-    const int total = QT * P.max_blocks;
-    for (int i = threadIdx.x; i < total; i += kThreads) {
-      const int ql = i / P.max_blocks, bi = i % P.max_blocks;
+    const int span = b_hi - b_lo;
+    for (int i = threadIdx.x; i < QT * span; i += kThreads) {
+      const int ql = i / span, bi = b_lo + i % span;
       const int q = q0 + ql;
       if (q < P.b.num_q && P.cand[(int64_t)q * P.max_blocks + bi] < 0) atomicMin(&ms->nb[ql], bi);
     }
@@ -411,11 +423,12 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
       if (P.cand) {
         const int nb = ms->nb[ql];
         len = (int64_t)nb * P.block;
-        ident = nb == 0 || P.cand[(int64_t)q * P.max_blocks + nb - 1] == nb - 1;
+        if (len > s_hi) len = s_hi;
+        ident = nb <= b_lo || P.cand[(int64_t)q * P.max_blocks + nb - 1] == nb - 1;
       }
       if (len > P.ld) {
         len = P.ld;
-        if (y == 0) err |= CSA2_DERR_LD;
+        if (P.cand || y == 0) err |= CSA2_DERR_LD;
       }
       ms->row_len[ql] = len;
       ms->n_vis[ql] = nv;

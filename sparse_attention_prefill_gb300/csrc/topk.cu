@@ -98,9 +98,17 @@ __device__ uint32_t select_topk(const Keys &keys, int64_t n, uint32_t k, SelectS
     __syncthreads();
     const uint32_t prefix = sh.prefix;
     const uint32_t hi_mask = shift == 24 ? 0u : (0xffffffffu << (shift + 8));
-    for (int64_t i = threadIdx.x; i < n; i += kThreads) {
-      const uint32_t key = keys(i);
-      if (key != 0u && (key & hi_mask) == prefix) atomicAdd(&sh.hist[(key >> shift) & 255u], 1u);
+    // warp-aggregated increments: the lanes holding the same digit add once
+    // (score keys cluster in a few exponent buckets, which would otherwise
+    // serialise on a handful of shared-memory counters)
+    for (int64_t i0 = 0; i0 < n; i0 += kThreads) {
+      const int64_t i = i0 + threadIdx.x;
+      uint32_t key = i < n ? keys(i) : 0u;
+      const bool take = key != 0u && (key & hi_mask) == prefix;
+      const uint32_t digit = take ? (key >> shift) & 255u : 256u;
+      const uint32_t peers = __match_any_sync(0xffffffffu, digit);
+      if (take && (threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1))
+        atomicAdd(&sh.hist[digit], (uint32_t)__popc(peers));
     }
     __syncthreads();
     // scan bins from the top digit down
@@ -203,7 +211,8 @@ __device__ void row_geometry(const Batch &b, int q, const int32_t *cand_blocks, 
 __global__ void __launch_bounds__(kThreads)
 topk_kernel(Batch b, const float *__restrict__ scores, int64_t ld, int k,
             const int32_t *__restrict__ cand_blocks, int block, int max_blocks,
-            int32_t *__restrict__ idx, int32_t *__restrict__ count, int32_t *__restrict__ d_err) {
+            int32_t *__restrict__ idx, int32_t *__restrict__ count, int32_t *__restrict__ d_err,
+            int64_t staged) {
   extern __shared__ uint32_t smem_keys[];
   __shared__ SelectShared sh;
   const int q = blockIdx.x;
@@ -215,7 +224,7 @@ topk_kernel(Batch b, const float *__restrict__ scores, int64_t ld, int k,
   int32_t *out = idx + (int64_t)q * k;
   auto emit = [&](int64_t s, uint32_t slot) { out[slot] = (int32_t)view.entry(s); };
   uint32_t got;
-  if (row_len <= kSmemKeys) {
+  if (row_len <= staged) {
     for (int64_t s = threadIdx.x; s < row_len; s += kThreads) smem_keys[s] = view(s);
     __syncthreads();
     got = select_topk(SmemKeys{smem_keys}, row_len, (uint32_t)k, sh, emit);
@@ -231,7 +240,7 @@ topk_kernel(Batch b, const float *__restrict__ scores, int64_t ld, int k,
 __global__ void __launch_bounds__(kThreads)
 candidate_blocks_kernel(Batch b, const float *__restrict__ scores, int64_t ld, int block,
                         int max_blocks, int32_t *__restrict__ blocks,
-                        int32_t *__restrict__ nblocks) {
+                        int32_t *__restrict__ nblocks, int64_t staged) {
   extern __shared__ uint32_t smem_keys[];
   __shared__ SelectShared sh;
   __shared__ int32_t chosen[kMaxSortBlocks];
@@ -251,7 +260,7 @@ candidate_blocks_kernel(Batch b, const float *__restrict__ scores, int64_t ld, i
   BlockView view{row, block, n_vis};
   auto emit = [&](int64_t bb, uint32_t slot) { chosen[slot] = (int32_t)bb; };
   const int64_t n = nb_all - 1;  // the latest block is kept outside the ranking
-  if (n <= kSmemKeys) {
+  if (n <= staged) {
     for (int64_t i = threadIdx.x; i < n; i += kThreads) smem_keys[i] = view(i);
     __syncthreads();
     select_topk(SmemKeys{smem_keys}, n, (uint32_t)(max_blocks - 1), sh, emit);
@@ -293,19 +302,24 @@ int topk_launch(const Batch &b, const float *scores, int64_t ld, int k,
                 int32_t *count, int32_t *blocks_out, int32_t *nblocks_out, int32_t *d_err,
                 cudaStream_t st) {
   if (b.num_q == 0) return CSA2_OK;
-  const size_t smem = (size_t)kSmemKeys * sizeof(uint32_t);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    cudaFuncSetAttribute(candidate_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)smem);
-    attr_set = true;
-  }
+  // shared memory only as large as the longest row can use (small rows then
+  // leave room for several CTAs per SM); rows longer than kSmemKeys stream
+  int64_t row_cap = cand_blocks ? (int64_t)max_blocks * block : ld;
+  if (row_cap > ld) row_cap = ld;
+  const int64_t staged = row_cap < kSmemKeys ? row_cap : kSmemKeys;
+  const size_t smem = (size_t)(staged > 0 ? staged : 1) * sizeof(uint32_t);
+  const int64_t nblk = (ld + block - 1) / block;
+  const size_t smem_b = (size_t)(nblk < kSmemKeys ? (nblk > 0 ? nblk : 1) : kSmemKeys) *
+                        sizeof(uint32_t);
+  cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   topk_kernel<<<b.num_q, kThreads, smem, st>>>(b, scores, ld, k, cand_blocks, block, max_blocks,
-                                               idx, count, d_err);
+                                               idx, count, d_err, staged);
   if (blocks_out) {
-    candidate_blocks_kernel<<<b.num_q, kThreads, smem, st>>>(b, scores, ld, block, max_blocks,
-                                                             blocks_out, nblocks_out);
+    cudaFuncSetAttribute(candidate_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)smem_b);
+    candidate_blocks_kernel<<<b.num_q, kThreads, smem_b, st>>>(
+        b, scores, ld, block, max_blocks, blocks_out, nblocks_out,
+        nblk < kSmemKeys ? nblk : (int64_t)kSmemKeys);
   }
   return launch_status();
 }
