@@ -90,10 +90,12 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
 }
 
 // Order-preserving map from float to uint32: larger float -> larger key.
-// NaN maps below every number; -inf just above NaN.
+// NaN maps below every number; -inf just above NaN; -0 and +0 share a key
+// (they compare equal, so their order is the entry id's).
 __device__ __forceinline__ uint32_t float_key(float f) {
   if (f != f) return 0u;
   uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 // key of -inf: every eligible score has a strictly larger key

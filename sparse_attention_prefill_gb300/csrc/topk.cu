@@ -7,31 +7,51 @@
 // maximum score, always keeping the block that holds the latest position.
 //
 // One CTA per query row.  Scores become order-preserving uint32 keys (0 marks
-// an ineligible element).  A 4-pass 8-bit radix select finds the k-th largest
-// key T; keys > T are emitted directly, and the k - #(> T) keys equal to T are
-// taken in index order by a block-wide ordered scan, which makes the result
-// exactly the pinned total order's top k.  Rows that fit in shared memory are
-// staged there once; longer rows are re-read from global memory (L2) in each
-// pass.  The same selection core ranks candidate blocks by block maximum, and
-// the chosen blocks are sorted ascending with a shared-memory bitonic sort.
+// an ineligible element); the selection is exactly the k largest keys, ties
+// by lowest position, which is the pinned total order's top k.
+//  - Rows of up to 16384 keys are held in registers (256 threads, KPT keys
+//    each, loaded together).  The k-th key of a strided sample, at a rank
+//    scaled to the sample plus a margin, bounds the threshold from below;
+//    the keys above it (typically ~1.5k) are compacted into shared memory and
+//    an 8-bit radix search finds the exact k-th key on that list alone.  A
+//    missed estimate falls back to the same search over the whole row.
+//  - Longer rows: a 4-pass radix select over the row staged in shared memory
+//    (or re-read from L2), then keys > T emitted directly and the keys equal
+//    to T taken in position order by a block-wide ordered scan.
+// Every sweep over a row loads several elements per thread before using any,
+// so that the loads overlap.  The same selection core ranks candidate blocks
+// by block maximum, and the chosen blocks are sorted ascending with a
+// shared-memory bitonic sort.
 #include "common.cuh"
 #include "kernels.cuh"
 
 namespace csa2 {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 512;        // CTA size for long rows and block ranking
 constexpr int kSmemKeys = 40960;      // staged row capacity (160 KB)
 constexpr int kMaxSortBlocks = 4096;  // max_blocks supported
+constexpr int kBatch = 8;             // elements per thread loaded together in a sweep
 
+// key of a score: order-preserving (larger score, larger key; -0 and +0
+// share a key), 0 for NaN and -inf (never selected)
+__device__ __forceinline__ uint32_t score_key(float f) {
+  f += 0.0f;  // -0 + 0 = +0
+  const uint32_t u = __float_as_uint(f);
+  const uint32_t k = u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+  return (f == f && k > neg_inf_key()) ? k : 0u;
+}
+
+template <int NT>
 struct SelectShared {
   uint32_t hist[256];
-  uint32_t warp_tot[kThreads / 32];
+  uint32_t warp_tot[NT / 32];
   uint32_t prefix, remaining, out_count, n_elig;
   int32_t nb;
 };
 
-// Block-wide exclusive scan of one uint32 per thread (kThreads threads).
+// Block-wide exclusive scan of one uint32 per thread (NT threads).
+template <int NT>
 __device__ uint32_t block_scan_u32(uint32_t v, uint32_t *warp_tot, uint32_t &total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t x = v;
@@ -44,110 +64,396 @@ __device__ uint32_t block_scan_u32(uint32_t v, uint32_t *warp_tot, uint32_t &tot
   if (lane == 31) warp_tot[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    uint32_t s = lane < kThreads / 32 ? warp_tot[lane] : 0u;
+    uint32_t s = lane < NT / 32 ? warp_tot[lane] : 0u;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
       if (lane >= o) s += y;
     }
-    if (lane < kThreads / 32) warp_tot[lane] = s;
+    if (lane < NT / 32) warp_tot[lane] = s;
   }
   __syncthreads();
-  total = warp_tot[kThreads / 32 - 1];
+  total = warp_tot[NT / 32 - 1];
   return (warp ? warp_tot[warp - 1] : 0u) + x - v;
 }
 
-// Select the k largest keys (key 0 = ineligible) of a virtual array of n keys,
-// ties by lowest index.  Calls emit(i) once for every selected index i (in no
-// particular order) and returns min(k, #eligible).
-template <class Keys, class Emit>
-__device__ uint32_t select_topk(const Keys &keys, int64_t n, uint32_t k, SelectShared &sh,
-                                Emit emit) {
-  // eligible count
-  uint32_t cnt = 0;
-  for (int64_t i = threadIdx.x; i < n; i += kThreads) cnt += keys(i) != 0u;
-  cnt = __reduce_add_sync(0xffffffffu, cnt);
-  if (threadIdx.x == 0) sh.n_elig = 0;
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) atomicAdd(&sh.n_elig, cnt);
-  __syncthreads();
-  const uint32_t n_elig = sh.n_elig;
-  if (n_elig <= k) {
-    // everything eligible is selected; keep index order for determinism
-    uint32_t base = 0;
-    for (int64_t c0 = 0; c0 < n; c0 += kThreads) {
-      const int64_t i = c0 + threadIdx.x;
-      const uint32_t f = (i < n && keys(i) != 0u) ? 1u : 0u;
-      uint32_t tot;
-      const uint32_t ex = block_scan_u32(f, sh.warp_tot, tot);
-      if (f) emit(i, base + ex);
-      base += tot;
-    }
-    __syncthreads();
-    return n_elig;
+// Warp-aggregated slot reservation: every lane with `take` gets a distinct
+// slot from *counter (one shared atomic per warp).
+__device__ __forceinline__ uint32_t warp_reserve(bool take, uint32_t *counter) {
+  const uint32_t m = __ballot_sync(0xffffffffu, take);
+  const int lane = threadIdx.x & 31;
+  uint32_t base = 0;
+  if (m) {
+    const int leader = __ffs(m) - 1;
+    if (lane == leader) base = atomicAdd(counter, (uint32_t)__popc(m));
+    base = __shfl_sync(0xffffffffu, base, leader);
   }
-  // radix select of the k-th largest key
+  return base + __popc(m & ((1u << lane) - 1u));
+}
+
+// Calls f(i, key) for i = i0 + u*NT + thread over a row of n elements of a
+// key source (keys.raw(i): the memory access, valid for any i < n;
+// keys.key(i, raw): the key, 0 = ineligible).  Each thread loads kBatch
+// elements before converting any, so their loads are in flight together.
+// Every thread makes the same number of calls (i >= n gives key 0), so f may
+// use warp-wide operations; per thread, i ascends.
+template <int NT, class Keys, class F>
+__device__ __forceinline__ void sweep(const Keys &keys, int64_t n, F f) {
+  for (int64_t i0 = 0; i0 < n; i0 += (int64_t)NT * kBatch) {
+    uint32_t r[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int64_t i = i0 + u * NT + threadIdx.x;
+      r[u] = keys.raw(i < n ? i : n - 1);
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int64_t i = i0 + u * NT + threadIdx.x;
+      f(i, i < n ? keys.key(i, r[u]) : 0u);
+    }
+  }
+}
+
+// Select the k largest keys (key 0 = ineligible) of a virtual array of n keys,
+// ties by lowest index.  Calls emit(i, slot) once for every selected index i
+// with distinct slots 0..min(k, #eligible)-1 and returns min(k, #eligible).
+template <int NT, class Keys, class Emit>
+__device__ uint32_t select_topk(const Keys &keys, int64_t n, uint32_t k, SelectShared<NT> &sh,
+                                Emit emit) {
+  // radix select of the k-th largest key; the first pass also counts the
+  // eligible keys (the histogram total)
   if (threadIdx.x == 0) {
     sh.prefix = 0;
     sh.remaining = k;
+    sh.out_count = 0;
+    sh.n_elig = 0;  // reused below: keys equal to the threshold
   }
-  __syncthreads();
+  uint32_t n_elig = 0;
 #pragma unroll 1
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += kThreads) sh.hist[i] = 0;
+    for (int i = threadIdx.x; i < 256; i += NT) sh.hist[i] = 0;
     __syncthreads();
     const uint32_t prefix = sh.prefix;
     const uint32_t hi_mask = shift == 24 ? 0u : (0xffffffffu << (shift + 8));
     // warp-aggregated increments: the lanes holding the same digit add once
-    // (score keys cluster in a few exponent buckets, which would otherwise
-    // serialise on a handful of shared-memory counters)
-    for (int64_t i0 = 0; i0 < n; i0 += kThreads) {
-      const int64_t i = i0 + threadIdx.x;
-      uint32_t key = i < n ? keys(i) : 0u;
+    sweep<NT>(keys, n, [&](int64_t, uint32_t key) {
       const bool take = key != 0u && (key & hi_mask) == prefix;
       const uint32_t digit = take ? (key >> shift) & 255u : 256u;
       const uint32_t peers = __match_any_sync(0xffffffffu, digit);
       if (take && (threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1))
         atomicAdd(&sh.hist[digit], (uint32_t)__popc(peers));
-    }
+    });
     __syncthreads();
     // scan bins from the top digit down
     const uint32_t remaining = sh.remaining;
     uint32_t h = threadIdx.x < 256 ? sh.hist[255 - threadIdx.x] : 0u;
     uint32_t tot;
-    const uint32_t ex = block_scan_u32(h, sh.warp_tot, tot);
+    const uint32_t ex = block_scan_u32<NT>(h, sh.warp_tot, tot);
+    if (shift == 24) {
+      n_elig = tot;
+      if (n_elig <= k) break;     // everything eligible is selected
+    }
     if (threadIdx.x < 256 && ex < remaining && ex + h >= remaining) {
       sh.prefix = prefix | ((uint32_t)(255 - threadIdx.x) << shift);
       sh.remaining = remaining - ex;
     }
     __syncthreads();
   }
+  if (n_elig <= k) {
+    sweep<NT>(keys, n, [&](int64_t i, uint32_t key) {
+      const uint32_t slot = warp_reserve(key != 0u, &sh.out_count);
+      if (key != 0u) emit(i, slot);
+    });
+    __syncthreads();
+    return n_elig;
+  }
   const uint32_t T = sh.prefix;
   const uint32_t need_eq = sh.remaining;  // how many keys == T to take
-  if (threadIdx.x == 0) sh.out_count = 0;
-  __syncthreads();
-  // keys above the threshold
-  for (int64_t i = threadIdx.x; i < n; i += kThreads) {
-    if (keys(i) > T) emit(i, atomicAdd(&sh.out_count, 1u));
-  }
+  // keys above the threshold (and a count of the keys equal to it)
+  uint32_t eq_local = 0;
+  sweep<NT>(keys, n, [&](int64_t i, uint32_t key) {
+    const uint32_t slot = warp_reserve(key > T, &sh.out_count);
+    if (key > T) emit(i, slot);
+    eq_local += key == T;
+  });
+  eq_local = __reduce_add_sync(0xffffffffu, eq_local);
+  if ((threadIdx.x & 31) == 0 && eq_local) atomicAdd(&sh.n_elig, eq_local);
   __syncthreads();
   const uint32_t n_gt = sh.out_count;
-  // keys equal to the threshold, lowest indices first
-  uint32_t base = 0;
-  for (int64_t c0 = 0; c0 < n && base < need_eq; c0 += kThreads) {
-    const int64_t i = c0 + threadIdx.x;
-    const uint32_t f = (i < n && keys(i) == T) ? 1u : 0u;
-    uint32_t tot;
-    const uint32_t ex = block_scan_u32(f, sh.warp_tot, tot);
-    if (f && base + ex < need_eq) emit(i, n_gt + base + ex);
-    base += tot;
+  const uint32_t n_eq = sh.n_elig;
+  if (n_eq == need_eq) {
+    // every key equal to the threshold is selected: no ordering needed
+    sweep<NT>(keys, n, [&](int64_t i, uint32_t key) {
+      const uint32_t slot = warp_reserve(key == T, &sh.out_count);
+      if (key == T) emit(i, slot);
+    });
+  } else {
+    // keys equal to the threshold, lowest indices first
+    uint32_t base = 0;
+    for (int64_t c0 = 0; c0 < n && base < need_eq; c0 += NT) {
+      const int64_t i = c0 + threadIdx.x;
+      const uint32_t f = (i < n && keys.key(i, keys.raw(i)) == T) ? 1u : 0u;
+      uint32_t tot;
+      const uint32_t ex = block_scan_u32<NT>(f, sh.warp_tot, tot);
+      if (f && base + ex < need_eq) emit(i, n_gt + base + ex);
+      base += tot;
+    }
   }
   __syncthreads();
   return k;
 }
 
-// Row view: the scores of query q as keys, in full mode (entries 0..len-1) or
-// pool mode (slots, mapped to entries through the candidate blocks).
+constexpr int kListCap = 4096;      // compacted candidates of one row (2x the largest k)
+constexpr int kSampleSlots = 4;      // register slots per thread in the threshold sample
+
+template <int NT>
+struct RegShared {
+  uint32_t hist[256];
+  uint32_t red[6][NT / 32];
+  uint32_t warp_tot[NT / 32];
+  uint32_t prefix, remaining, bin_count, out_count;
+  uint32_t list_key[kListCap];
+  int32_t list_pos[kListCap];
+};
+
+__device__ __forceinline__ uint32_t keep_above(uint32_t x, int b) {  // bits >= b of x
+  return b >= 32 ? 0u : (x >> b) << b;
+}
+
+// Block-wide radix search for the k-th largest of the keys that `each` visits
+// (each(f) calls f(x) on every key this thread holds; 0 = ineligible), given
+// bounds mn <= x <= mx on the eligible keys and at least k of them.  The 8-bit
+// digits start at the highest bit in which mn and mx differ (the bits above
+// are common to every key in between) and the search stops as soon as the
+// k-th key's bin is taken whole.  Result: the selection is every key >= lo,
+// lo = whole ? prefix : prefix + 1, plus (if !whole) `rem` keys == prefix.
+// One warp scans the 256 bins and clears them; the histogram is all zero on
+// entry and on exit.
+template <int NT, class Each>
+__device__ void radix_kth(Each each, uint32_t mn, uint32_t mx, uint32_t k, RegShared<NT> &sh,
+                          uint32_t &prefix, uint32_t &rem, bool &whole) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int hb = mx == mn ? 0 : 32 - __clz(mx ^ mn);
+  prefix = keep_above(mx, hb);
+  rem = k;
+  whole = false;
+  while (hb > 0) {
+    const int width = hb < 8 ? hb : 8;
+    const int shift = hb - width;
+    const uint32_t dmask = (1u << width) - 1u;
+    const uint32_t pre = prefix;
+    each([&](uint32_t x) {
+      if (x != 0u && keep_above(x, hb) == pre) atomicAdd(&sh.hist[(x >> shift) & dmask], 1u);
+    });
+    __syncthreads();
+    if (warp == 0) {
+      // lane l holds bins top-8l .. top-8l-7 (descending key order)
+      const int top = (int)dmask;
+      uint32_t h[8], sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int bin = top - (lane * 8 + i);
+        h[i] = bin >= 0 ? sh.hist[bin] : 0u;
+        if (bin >= 0) sh.hist[bin] = 0u;
+        sum += h[i];
+      }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      uint32_t e = incl - sum;
+      if (e < rem && rem <= incl) {
+        bool found = false;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (!found && e + h[i] >= rem) {
+            found = true;
+            sh.prefix = pre | ((uint32_t)(top - (lane * 8 + i)) << shift);
+            sh.remaining = rem - e;
+            sh.bin_count = h[i];
+          }
+          e += h[i];
+        }
+      }
+    }
+    __syncthreads();
+    prefix = sh.prefix;
+    rem = sh.remaining;
+    const uint32_t n_eq = sh.bin_count;
+    hb = shift;
+    if (n_eq == rem) {
+      whole = true;
+      break;
+    }
+  }
+}
+
+// Selection for a row held in registers: thread t owns positions t + j*NT
+// (key[j], 0 = ineligible; slots j >= jn hold no keys).
+//  1. Count the eligible keys; if at most k, all are selected.
+//  2. Rows of more than 2*kSampleSlots keys per thread: find the k-th key of a
+//     strided sample (kSampleSlots slots per thread), at a rank scaled to the
+//     sample with a margin, and compact every key >= that estimate into a
+//     shared-memory list.  With between k and kListCap keys listed, the exact
+//     search runs on the list alone; otherwise (a rare miss of the estimate)
+//     on the whole row.
+//  3. Emit the keys >= lo; keys equal to the threshold, if only some of them
+//     are taken, go in position order by a block scan over the row.
+template <int NT, int KPT, class Emit>
+__device__ uint32_t select_topk_regs(const uint32_t (&key)[KPT], int jn, uint32_t k,
+                                     RegShared<NT> &sh, Emit emit) {
+  constexpr int kStride = KPT / kSampleSlots > 0 ? KPT / kSampleSlots : 1;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  uint32_t cnt = 0, mx = 0, s_cnt = 0, s_mn = 0xffffffffu, s_mx = 0;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    if (j >= jn) break;
+    const uint32_t x = key[j];
+    cnt += x != 0u;
+    mx = max(mx, x);
+    if (j % kStride == 0) {
+      s_cnt += x != 0u;
+      s_mn = min(s_mn, x ? x : 0xffffffffu);
+      s_mx = max(s_mx, x);
+    }
+  }
+  cnt = __reduce_add_sync(0xffffffffu, cnt);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  s_cnt = __reduce_add_sync(0xffffffffu, s_cnt);
+  s_mn = __reduce_min_sync(0xffffffffu, s_mn);
+  s_mx = __reduce_max_sync(0xffffffffu, s_mx);
+  if (lane == 0) {
+    sh.red[0][warp] = cnt;
+    sh.red[2][warp] = mx;
+    sh.red[3][warp] = s_cnt;
+    sh.red[4][warp] = s_mn;
+    sh.red[5][warp] = s_mx;
+  }
+  for (int i = t; i < 256; i += NT) sh.hist[i] = 0;
+  if (t == 0) sh.out_count = 0;
+  __syncthreads();
+  uint32_t n_elig = 0;
+  cnt = 0;
+  mx = 0;
+  s_mn = 0xffffffffu;
+  s_mx = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    n_elig += sh.red[0][w];
+    mx = max(mx, sh.red[2][w]);
+    cnt += sh.red[3][w];
+    s_mn = min(s_mn, sh.red[4][w]);
+    s_mx = max(s_mx, sh.red[5][w]);
+  }
+  if (n_elig <= k) {  // everything eligible is selected
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      if (j >= jn) break;
+      const bool take = key[j] != 0u;
+      const uint32_t slot = warp_reserve(take, &sh.out_count);
+      if (take) emit(j * NT + t, slot);
+    }
+    __syncthreads();
+    return n_elig;
+  }
+  uint32_t prefix, rem;
+  bool whole;
+  bool listed = false;
+  uint32_t n_list = 0;
+  if (jn > 2 * kSampleSlots && cnt > 0) {
+    // sample rank matching rank k of the row, plus a margin (~3 sigma)
+    const uint64_t r0 = ((uint64_t)k * cnt * 13) / (10ull * n_elig) + 16;
+    const uint32_t rs = (uint32_t)(r0 < cnt ? r0 : cnt);
+    radix_kth<NT>(
+        [&](auto f) {
+#pragma unroll
+          for (int j = 0; j < KPT; j += kStride)
+            if (j < jn) f(key[j]);
+        },
+        s_mn, s_mx, rs, sh, prefix, rem, whole);
+    // the sample's rs-th key (an eligible key, so t_est >= 1): keys >= t_est
+    // are counted, offsets taken by a block scan, and written if they fit
+    const uint32_t t_est = prefix;
+    uint32_t mine = 0;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      if (j >= jn) break;
+      mine += key[j] >= t_est;
+    }
+    uint32_t off = block_scan_u32<NT>(mine, sh.warp_tot, n_list);
+    if (n_list >= k && n_list <= (uint32_t)kListCap) {
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) {
+        if (j >= jn) break;
+        if (key[j] >= t_est) {
+          sh.list_key[off] = key[j];
+          sh.list_pos[off] = j * NT + t;
+          ++off;
+        }
+      }
+      __syncthreads();
+      // every key of the selection is >= t_est, hence listed
+      listed = true;
+      radix_kth<NT>(
+          [&](auto f) {
+            for (int i = t; i < (int)n_list; i += NT) f(sh.list_key[i]);
+          },
+          t_est, mx, k, sh, prefix, rem, whole);
+    }
+  }
+  if (!listed) {
+    // every eligible key is >= 1
+    radix_kth<NT>(
+        [&](auto f) {
+#pragma unroll
+          for (int j = 0; j < KPT; ++j)
+            if (j < jn) f(key[j]);
+        },
+        1u, mx, k, sh, prefix, rem, whole);
+  }
+  const uint32_t lo = whole ? prefix : prefix + 1u;
+  if (listed) {
+    for (int i0 = 0; i0 < (int)n_list; i0 += NT) {
+      const int i = i0 + t;
+      const uint32_t x = i < (int)n_list ? sh.list_key[i] : 0u;
+      const bool take = x != 0u && x >= lo;
+      const uint32_t slot = warp_reserve(take, &sh.out_count);
+      if (take) emit(sh.list_pos[i], slot);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      if (j >= jn) break;
+      const uint32_t x = key[j];
+      const bool take = x != 0u && x >= lo;
+      const uint32_t slot = warp_reserve(take, &sh.out_count);
+      if (take) emit(j * NT + t, slot);
+    }
+  }
+  if (!whole) {
+    // keys equal to the threshold, lowest positions first (position order is
+    // slot-major: j, then thread)
+    const uint32_t base_slot = k - rem;
+    uint32_t base = 0;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      if (j >= jn || base >= rem) break;
+      const uint32_t f = key[j] == prefix ? 1u : 0u;
+      uint32_t tot;
+      const uint32_t ex = block_scan_u32<NT>(f, sh.warp_tot, tot);
+      if (f && base + ex < rem) emit(j * NT + t, base_slot + base + ex);
+      base += tot;
+    }
+  }
+  __syncthreads();
+  return k;
+}
+
+// Key sources (see sweep()).  Row view: the scores of query q, in full mode
+// (entries 0..len-1) or pool mode (slots, mapped to entries through the
+// query's candidate blocks, read from a shared-memory copy).
 struct RowView {
   const float *row;
   const int32_t *cand;  // candidate blocks of this query or nullptr
@@ -156,16 +462,19 @@ struct RowView {
   __device__ __forceinline__ int64_t entry(int64_t s) const {
     return cand ? (int64_t)cand[s / block] * block + s % block : s;
   }
-  __device__ __forceinline__ uint32_t operator()(int64_t s) const {
+  __device__ __forceinline__ uint32_t raw(int64_t s) const {
+    return __float_as_uint(__ldg(row + s));
+  }
+  __device__ __forceinline__ uint32_t key(int64_t s, uint32_t r) const {
     if (cand && entry(s) >= n_vis) return 0u;
-    const uint32_t key = float_key(__ldg(row + s));
-    return key > neg_inf_key() ? key : 0u;
+    return score_key(__uint_as_float(r));
   }
 };
 
 struct SmemKeys {
   const uint32_t *k;
-  __device__ __forceinline__ uint32_t operator()(int64_t i) const { return k[i]; }
+  __device__ __forceinline__ uint32_t raw(int64_t i) const { return k[i]; }
+  __device__ __forceinline__ uint32_t key(int64_t, uint32_t r) const { return r; }
 };
 
 // Block view: key of block b = max key over its visible entries, plus one, so
@@ -174,17 +483,21 @@ struct BlockView {
   const float *row;
   int block;
   int64_t n_vis;
-  __device__ __forceinline__ uint32_t operator()(int64_t b) const {
+  __device__ __forceinline__ uint32_t raw(int64_t b) const {
     uint32_t m = 0;
     const int64_t j1 = min((b + 1) * block, n_vis);
     for (int64_t j = b * block; j < j1; ++j) m = max(m, float_key(__ldg(row + j)));
     return m + 1u;
   }
+  __device__ __forceinline__ uint32_t key(int64_t, uint32_t r) const { return r; }
 };
 
+// Visible entries and row length of query q; in pool mode the query's
+// candidate blocks are also copied to scand (the first -1 ends the row).
+template <int NT>
 __device__ void row_geometry(const Batch &b, int q, const int32_t *cand_blocks, int block,
-                             int max_blocks, int64_t ld, int64_t &n_vis, int64_t &row_len,
-                             int &err, SelectShared &sh) {
+                             int max_blocks, int64_t ld, int32_t *scand, int64_t &n_vis,
+                             int64_t &row_len, int &err, SelectShared<NT> &sh) {
   const int r = b.q_req[q];
   n_vis = n_visible(b.q_pos[q], b.ratio);
   if (n_vis > b.kv_len[r]) {
@@ -195,8 +508,20 @@ __device__ void row_geometry(const Batch &b, int q, const int32_t *cand_blocks, 
     if (threadIdx.x == 0) sh.nb = max_blocks;
     __syncthreads();
     const int32_t *cb = cand_blocks + (int64_t)q * max_blocks;
-    for (int i = threadIdx.x; i < max_blocks; i += kThreads)
-      if (cb[i] < 0) atomicMin(&sh.nb, i);
+    for (int i0 = 0; i0 < max_blocks; i0 += NT * kBatch) {
+      int32_t v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        v[u] = __ldg(cb + min(i0 + u * NT + (int)threadIdx.x, max_blocks - 1));
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int i = i0 + u * NT + threadIdx.x;
+        if (i < max_blocks) {
+          scand[i] = v[u];
+          if (v[u] < 0) atomicMin(&sh.nb, i);
+        }
+      }
+    }
     __syncthreads();
     row_len = (int64_t)sh.nb * block;
   } else {
@@ -208,33 +533,63 @@ __device__ void row_geometry(const Batch &b, int q, const int32_t *cand_blocks, 
   }
 }
 
-__global__ void __launch_bounds__(kThreads)
+// minimum residency chosen so the key registers do not spill
+template <int NT, int KPT>
+__global__ void __launch_bounds__(NT, NT >= 512 ? 1 : KPT >= 64 ? 2 : KPT >= 32 ? 3 : 4)
 topk_kernel(Batch b, const float *__restrict__ scores, int64_t ld, int k,
             const int32_t *__restrict__ cand_blocks, int block, int max_blocks,
             int32_t *__restrict__ idx, int32_t *__restrict__ count, int32_t *__restrict__ d_err,
             int64_t staged) {
-  extern __shared__ uint32_t smem_keys[];
-  __shared__ SelectShared sh;
+  // dynamic shared memory: [staged keys (staged)][candidate blocks (pool mode)]
+  extern __shared__ __align__(16) uint32_t smem_dyn[];
+  uint32_t *skeys = smem_dyn;
+  int32_t *scand = reinterpret_cast<int32_t *>(smem_dyn + staged);
+  __shared__ SelectShared<NT> sh;
+  __shared__ RegShared<NT> rsh;
   const int q = blockIdx.x;
   int err = 0;
   int64_t n_vis, row_len;
-  row_geometry(b, q, cand_blocks, block, max_blocks, ld, n_vis, row_len, err, sh);
-  RowView view{scores + (int64_t)q * ld, cand_blocks ? cand_blocks + (int64_t)q * max_blocks : nullptr,
-                block, n_vis};
+  row_geometry(b, q, cand_blocks, block, max_blocks, ld, scand, n_vis, row_len, err, sh);
+  RowView view{scores + (int64_t)q * ld, cand_blocks ? scand : nullptr, block, n_vis};
   int32_t *out = idx + (int64_t)q * k;
   auto emit = [&](int64_t s, uint32_t slot) { out[slot] = (int32_t)view.entry(s); };
   uint32_t got;
-  if (row_len <= staged) {
-    for (int64_t s = threadIdx.x; s < row_len; s += kThreads) smem_keys[s] = view(s);
+  if (row_len <= (int64_t)NT * KPT) {
+    uint32_t key[KPT];
+    const int rl = (int)row_len;
+    const int jn = (rl + NT - 1) / NT;
+    // every load first, at clamped (always valid) addresses, then the keys:
+    // no branch separates the loads, so they are all in flight together
+#pragma unroll
+    for (int j = 0; j < KPT; ++j)
+      key[j] = j < jn ? view.raw(min(j * NT + (int)threadIdx.x, rl - 1)) : 0u;
+    if (view.cand) {
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) {
+        const int s = j * NT + threadIdx.x;
+        key[j] = s < rl ? view.key(s, key[j]) : 0u;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) {
+        const int s = j * NT + threadIdx.x;
+        key[j] = s < rl ? score_key(__uint_as_float(key[j])) : 0u;
+      }
+    }
+    got = select_topk_regs<NT, KPT>(key, jn, (uint32_t)k, rsh, emit);
+  } else if (row_len <= staged) {
+    sweep<NT>(view, row_len, [&](int64_t s, uint32_t x) {
+      if (s < row_len) skeys[s] = x;
+    });
     __syncthreads();
-    got = select_topk(SmemKeys{smem_keys}, row_len, (uint32_t)k, sh, emit);
+    got = select_topk<NT>(SmemKeys{skeys}, row_len, (uint32_t)k, sh, emit);
   } else {
-    got = select_topk(view, row_len, (uint32_t)k, sh, emit);
+    got = select_topk<NT>(view, row_len, (uint32_t)k, sh, emit);
   }
-  for (int i = (int)got + threadIdx.x; i < k; i += kThreads) out[i] = -1;
+  for (int i = (int)got + threadIdx.x; i < k; i += NT) out[i] = -1;
   if (threadIdx.x == 0) count[q] = (int32_t)got;
   err = __reduce_or_sync(0xffffffffu, err);
-  if ((threadIdx.x & 31) == 0 && threadIdx.x == 0) raise_err(d_err, err);
+  if (threadIdx.x == 0) raise_err(d_err, err);
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -242,7 +597,7 @@ candidate_blocks_kernel(Batch b, const float *__restrict__ scores, int64_t ld, i
                         int max_blocks, int32_t *__restrict__ blocks,
                         int32_t *__restrict__ nblocks, int64_t staged) {
   extern __shared__ uint32_t smem_keys[];
-  __shared__ SelectShared sh;
+  __shared__ SelectShared<kThreads> sh;
   __shared__ int32_t chosen[kMaxSortBlocks];
   const int q = blockIdx.x;
   const int r = b.q_req[q];
@@ -261,11 +616,13 @@ candidate_blocks_kernel(Batch b, const float *__restrict__ scores, int64_t ld, i
   auto emit = [&](int64_t bb, uint32_t slot) { chosen[slot] = (int32_t)bb; };
   const int64_t n = nb_all - 1;  // the latest block is kept outside the ranking
   if (n <= staged) {
-    for (int64_t i = threadIdx.x; i < n; i += kThreads) smem_keys[i] = view(i);
+    sweep<kThreads>(view, n, [&](int64_t i, uint32_t x) {
+      if (i < n) smem_keys[i] = x;
+    });
     __syncthreads();
-    select_topk(SmemKeys{smem_keys}, n, (uint32_t)(max_blocks - 1), sh, emit);
+    select_topk<kThreads>(SmemKeys{smem_keys}, n, (uint32_t)(max_blocks - 1), sh, emit);
   } else {
-    select_topk(view, n, (uint32_t)(max_blocks - 1), sh, emit);
+    select_topk<kThreads>(view, n, (uint32_t)(max_blocks - 1), sh, emit);
   }
   // add the latest block, pad to a power of two and sort ascending
   int pow2 = 1;
@@ -302,18 +659,26 @@ int topk_launch(const Batch &b, const float *scores, int64_t ld, int k,
                 int32_t *count, int32_t *blocks_out, int32_t *nblocks_out, int32_t *d_err,
                 cudaStream_t st) {
   if (b.num_q == 0) return CSA2_OK;
-  // shared memory only as large as the longest row can use (small rows then
-  // leave room for several CTAs per SM); rows longer than kSmemKeys stream
+  // rows of up to 16384 keys are held in registers (KPT keys per thread,
+  // sized to the longest possible row); longer rows are staged in shared
+  // memory up to kSmemKeys, else re-read from L2 in each pass
   int64_t row_cap = cand_blocks ? (int64_t)max_blocks * block : ld;
   if (row_cap > ld) row_cap = ld;
-  const int64_t staged = row_cap < kSmemKeys ? row_cap : kSmemKeys;
-  const size_t smem = (size_t)(staged > 0 ? staged : 1) * sizeof(uint32_t);
   const int64_t nblk = (ld + block - 1) / block;
   const size_t smem_b = (size_t)(nblk < kSmemKeys ? (nblk > 0 ? nblk : 1) : kSmemKeys) *
                         sizeof(uint32_t);
-  cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  topk_kernel<<<b.num_q, kThreads, smem, st>>>(b, scores, ld, k, cand_blocks, block, max_blocks,
-                                               idx, count, d_err, staged);
+  auto launch = [&](auto kern, int nt, int64_t staged) {
+    const size_t smem = (size_t)(staged + (cand_blocks ? max_blocks : 0)) * sizeof(uint32_t);
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    kern<<<b.num_q, nt, smem, st>>>(b, scores, ld, k, cand_blocks, block, max_blocks, idx, count,
+                                    d_err, staged);
+  };
+  if (row_cap <= 256 * 4) launch(topk_kernel<256, 4>, 256, 0);
+  else if (row_cap <= 256 * 8) launch(topk_kernel<256, 8>, 256, 0);
+  else if (row_cap <= 256 * 16) launch(topk_kernel<256, 16>, 256, 0);
+  else if (row_cap <= 256 * 32) launch(topk_kernel<256, 32>, 256, 0);
+  else if (row_cap <= 256 * 64) launch(topk_kernel<256, 64>, 256, 0);
+  else launch(topk_kernel<kThreads, 32>, kThreads, row_cap < kSmemKeys ? row_cap : kSmemKeys);
   if (blocks_out) {
     cudaFuncSetAttribute(candidate_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem_b);

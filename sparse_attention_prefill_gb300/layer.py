@@ -40,7 +40,9 @@ class LayerRunner:
         self.nq = nq
         self.d_err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.scores = torch.empty((nq, max(1, w.ld)), dtype=torch.float32, device=dev)
-        pool_len = w.max_blocks * w.block
+        # pool rows hold at most min(max_blocks, ceil(ld / block)) blocks: the
+        # candidate blocks are distinct blocks of a visible range of <= ld entries
+        pool_len = min(w.max_blocks, -(-max(1, w.ld) // w.block)) * w.block
         self.pool_scores = torch.empty((nq, pool_len), dtype=torch.float32, device=dev)
         self.idx: Dict[str, torch.Tensor] = {}
         self.count: Dict[str, torch.Tensor] = {}

@@ -106,8 +106,9 @@ def _layer_parity(w, runner, layer, rows, mode, pool=None, given_idx=None, win_l
         if pool is not None:
             same_pool = (npy(runner.blocks[rows]) == pool).all(1)
             assert same_pool.mean() >= 0.99, same_pool.mean()
-            ld = pool.shape[1] * w.block
-            ref_s, tol, _ = _oracle_scores(w, layer, b_or, rows, ld, cand=pool)
+            ld = runner.pool_scores.shape[1]
+            ref_s, tol, oerr = _oracle_scores(w, layer, b_or, rows, ld, cand=pool)
+            assert oerr & 16 == 0     # no row longer than the stride (the LD flag)
             sel = torch.from_numpy(np.nonzero(same_pool)[0]).to(DEV)
             _check_scores(runner.pool_scores[rows][sel], torch.arange(len(sel), device=DEV),
                           ref_s[same_pool], tol[same_pool])

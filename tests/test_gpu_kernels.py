@@ -168,6 +168,33 @@ def test_topk_full_mode_bit_exact(n, k):
     topk_sets_match(idx, cnt, ref_idx, ref_cnt)
 
 
+@pytest.mark.parametrize("n,k", [(1024, 512), (2048, 512), (4000, 512), (8192, 512), (16384, 512),
+                                 (16384, 2048), (6000, 1)])
+def test_topk_special_rows_bit_exact(n, k):
+    """Rows of every register-path size with degenerate contents: all keys
+    equal, ties straddling the k-th key, fewer than k eligible entries, one
+    eligible entry, dense coarse-grid scores, and -0/+0 (equal scores, so
+    entry order decides) at the k-th key."""
+    rng = np.random.default_rng(7 * n + k)
+    q_pos = [n - 1] * 7 + [k - 1, n // 3, n - 1]
+    s = (np.round(rng.standard_normal((len(q_pos), n)) * 4) / 4).astype(np.float32)
+    s[0, :] = 1.5                                         # all equal
+    s[1, :] = np.where(rng.random(n) < 0.5, 2.0, -1.0)    # two values
+    s[2, :] = np.nan
+    s[2, rng.choice(n, min(n, k // 2 + 1), replace=False)] = 3.0  # few eligible, tied
+    s[3, :] = -np.inf
+    s[3, n // 2] = 0.0                                    # one eligible
+    s[4, :] = rng.standard_normal(n).astype(np.float32)   # continuous
+    s[5, :] = -np.abs(s[5, :]) - 1e-3                     # negative keys only
+    s[6, :] = np.float32(1e-40)                           # subnormal, all equal
+    s[9, :] = np.where(rng.random(n) < 0.5, np.float32(-0.0), np.float32(0.0))
+    s[9, rng.choice(n, k // 2, replace=False)] = 1.0      # -0 and +0 tie at the k-th key
+    b = _sel_batch(q_pos, n)
+    ref_idx, ref_cnt, _ = O.topk(np_batch(b), s, k)
+    idx, cnt = S.topk(_to(b), torch.from_numpy(s).to(DEV), k)
+    topk_sets_match(idx, cnt, ref_idx, ref_cnt)
+
+
 def test_topk_pool_mode_bit_exact():
     rng = np.random.default_rng(9)
     q_pos = [16383, 9000, 100, 16390]

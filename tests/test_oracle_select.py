@@ -40,6 +40,14 @@ def test_topk_brute_force_with_ties_nan_inf(seed):
         assert (idx[q, count[q]:] == -1).all()
 
 
+def test_topk_signed_zeros_tie_by_entry():
+    """-0 and +0 are equal scores, so the entry id orders them."""
+    row = np.array([-0.0, 1.0, 0.0, -0.0, 0.0, -1.0], np.float32)
+    idx, count, err = O.topk(_batch([5]), row[None, :], 3)
+    assert err == 0 and count[0] == 3
+    assert idx[0].tolist() == [1, 0, 2]
+
+
 def test_topk_invariants_and_short_rows():
     rng = np.random.default_rng(7)
     s = rng.standard_normal((3, 2000)).astype(np.float32)
