@@ -217,68 +217,105 @@ __device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two) {
   return h2;
 }
 
-// one pipeline step: channels [128*pair, 128*pair+128) of the 128 rows of a chunk
-constexpr int kItemsPerStep = kRowsPerChunk * 8;  // 8 segments of 16 channels per row
-constexpr int kItemsPerThread = (kItemsPerStep + kProducerThreads - 1) / kProducerThreads;
+// One pipeline step: channels [128*pair, 128*pair+128) of the 128 rows of a
+// chunk, as 1024 items of 16 channels.  Item ptid + 28*8*i of a producer
+// thread is segment ptid%8 (16 channels) of row ptid/8 + 28i: the segment is
+// the same for every item and step of a thread, so the per-thread address
+// parts are fixed once per query and only the row changes per item.
+constexpr int kRowStride = kProducerThreads / 8;   // rows between a thread's items
+constexpr int kItemsPerThread = (kRowsPerChunk + kRowStride - 1) / kRowStride;
+static_assert(kProducerThreads % 8 == 0, "segment fixed per thread");
 
-__device__ __forceinline__ void load_step(const Params &P, const int *list, const Rows &rows,
-                                          int64_t kv0, int chunk, int pair, int ptid,
-                                          Item (&it)[kItemsPerThread]) {
-  // addresses first (branch-free: rows without data read the first SWA row
-  // and are zeroed afterwards), then every load of the step in one batch
-  const uint8_t *src[kItemsPerThread];
-  const float *sc[kItemsPerThread];
+// Per-thread, per-query source bases (segment offset folded in).
+struct Src {
+  const uint8_t *sel_b;   // row kv0 of the pool
+  const float *sel_s;
+  const uint8_t *win_b;   // first window row of the SWA buffer
+  const float *win_s;
+  const uint8_t *dummy_b; // a readable row for rows past the end (masked when stored)
+  const float *dummy_s;
+  int64_t nsel, nrows;
+};
+
+__device__ __forceinline__ void load_step(const int *list, const Src &S, int row0, int chunk,
+                                          int pair, Item (&it)[kItemsPerThread]) {
+  const int64_t r0 = (int64_t)chunk * kRowsPerChunk;
+  const int cb = pair * 128, sb = pair * 4;
+  if (r0 + kRowsPerChunk <= S.nsel) {          // every row selected
 #pragma unroll
-  for (int i = 0; i < kItemsPerThread; ++i) {
-    const int item = ptid + i * kProducerThreads;
-    const int row = (item >> 3) & (kRowsPerChunk - 1), seg = item & 7;
-    const int64_t ri = (int64_t)chunk * kRowsPerChunk + row;
-    const int d = pair * 128 + seg * 16;
-    const bool sel = ri < rows.nsel;
-    const bool win = !sel && ri < rows.nsel + rows.nwin;
-    const bool valid = item < kItemsPerStep && (sel || win);
-    const int64_t g = sel ? kv0 + list[sel ? ri : 0] : rows.win_first + (ri - rows.nsel);
-    const uint8_t *base = sel ? P.kv_fp8 : P.swa_fp8;
-    const float *sbase = sel ? P.kv_scale : P.swa_scale;
-    src[i] = valid ? base + g * kDim + d : P.swa_fp8;
-    sc[i] = valid ? sbase + g * (kDim / 32) + d / 32 : P.swa_scale;
-  }
-  // no use of the loaded values here: the mask is applied when the step is
-  // stored, so the loads stay in flight while earlier steps are written
+    for (int i = 0; i < kItemsPerThread; ++i) {
+      if (row0 + i * kRowStride < kRowsPerChunk) {
+        const int64_t j = list[r0 + row0 + i * kRowStride];
+        it[i].codes = __ldg(reinterpret_cast<const uint4 *>(S.sel_b + j * kDim + cb));
+        it[i].scale = __ldg(S.sel_s + j * (kDim / 32) + sb);
+      }
+    }
+  } else if (r0 >= S.nsel && r0 + kRowsPerChunk <= S.nrows) {   // every row in the window
 #pragma unroll
-  for (int i = 0; i < kItemsPerThread; ++i) {
-    it[i].codes = __ldg(reinterpret_cast<const uint4 *>(src[i]));
-    it[i].scale = __ldg(sc[i]);
+    for (int i = 0; i < kItemsPerThread; ++i) {
+      if (row0 + i * kRowStride < kRowsPerChunk) {
+        const int64_t w = r0 + row0 + i * kRowStride - S.nsel;
+        it[i].codes = __ldg(reinterpret_cast<const uint4 *>(S.win_b + w * kDim + cb));
+        it[i].scale = __ldg(S.win_s + w * (kDim / 32) + sb);
+      }
+    }
+  } else {                                     // boundary or last chunk
+#pragma unroll
+    for (int i = 0; i < kItemsPerThread; ++i) {
+      if (row0 + i * kRowStride < kRowsPerChunk) {
+        const int64_t ri = r0 + row0 + i * kRowStride;
+        const uint8_t *b;
+        const float *sc;
+        if (ri < S.nsel) {
+          const int64_t j = list[ri];
+          b = S.sel_b + j * kDim;
+          sc = S.sel_s + j * (kDim / 32);
+        } else if (ri < S.nrows) {
+          b = S.win_b + (ri - S.nsel) * kDim;
+          sc = S.win_s + (ri - S.nsel) * (kDim / 32);
+        } else {
+          b = S.dummy_b;
+          sc = S.dummy_s;
+        }
+        it[i].codes = __ldg(reinterpret_cast<const uint4 *>(b + cb));
+        it[i].scale = __ldg(sc + sb);
+      }
+    }
   }
 }
 
-__device__ __forceinline__ void store_step(uint8_t *R, int pair, int ptid, int64_t ri0,
-                                           int64_t nrows, const Item (&it)[kItemsPerThread]) {
+// Dequantise a step into R.  off[i][0..1]: byte offsets (pair 0) of the two
+// 16-byte stores of item i.  The 8 threads of a store phase cover one row's 8
+// segments; segments 0-3 and 4-7 fall in two column blocks whose 16-byte
+// chunks share banks, so threads of segments 4-7 store their upper half
+// first: every phase then touches 8 distinct chunk positions.
+template <bool kMasked>
+__device__ __forceinline__ void store_step(uint8_t *R, int pair, bool swap, int row0,
+                                           const uint32_t (&off)[kItemsPerThread][2],
+                                           int64_t valid_rows, const Item (&it)[kItemsPerThread]) {
+  uint8_t *Rb = R + pair * 2 * kRBlock;
 #pragma unroll
   for (int i = 0; i < kItemsPerThread; ++i) {
-    const int item = ptid + i * kProducerThreads;
-    if (item < kItemsPerStep) {
-      const int row = item >> 3, seg = item & 7;
-      const int d = pair * 128 + seg * 16;
-      const bool valid = ri0 + row < nrows;
-      const __half2 s2 = __float2half2_rn(valid ? it[i].scale : 0.f);
-      const uint32_t w[4] = {valid ? it[i].codes.x : 0u, valid ? it[i].codes.y : 0u,
-                             valid ? it[i].codes.z : 0u, valid ? it[i].codes.w : 0u};
-      uint32_t h[8];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        h[2 * j] = hmul2_u32(e4m3x2_f16x2(w[j] & 0xffffu), s2);
-        h[2 * j + 1] = hmul2_u32(e4m3x2_f16x2(w[j] >> 16), s2);
+    if (row0 + i * kRowStride < kRowsPerChunk) {
+      uint4 cd = it[i].codes;
+      float sc = it[i].scale;
+      if (kMasked && row0 + i * kRowStride >= valid_rows) {
+        cd = make_uint4(0, 0, 0, 0);
+        sc = 0.f;
       }
-      // the 8 threads of a store phase cover one row's 8 segments; segments
-      // 0-3 and 4-7 fall in two column blocks whose 16-byte chunks share banks,
-      // so the second block writes its halves in the opposite order: every
-      // phase then touches 8 distinct chunk positions (no bank conflict)
-      const uint4 lo = make_uint4(h[0], h[1], h[2], h[3]);
-      const uint4 hi = make_uint4(h[4], h[5], h[6], h[7]);
-      const bool swap = (seg & 4) != 0;
-      *reinterpret_cast<uint4 *>(R + sw128_offset(row, swap ? d + 8 : d, kRBlock)) = swap ? hi : lo;
-      *reinterpret_cast<uint4 *>(R + sw128_offset(row, swap ? d : d + 8, kRBlock)) = swap ? lo : hi;
+      const __half2 s2 = __float2half2_rn(sc);
+      const uint32_t a = swap ? cd.z : cd.x, b = swap ? cd.w : cd.y;
+      const uint32_t c = swap ? cd.x : cd.z, d = swap ? cd.y : cd.w;
+      const uint4 first = make_uint4(hmul2_u32(e4m3x2_f16x2(a & 0xffffu), s2),
+                                     hmul2_u32(e4m3x2_f16x2(a >> 16), s2),
+                                     hmul2_u32(e4m3x2_f16x2(b & 0xffffu), s2),
+                                     hmul2_u32(e4m3x2_f16x2(b >> 16), s2));
+      const uint4 second = make_uint4(hmul2_u32(e4m3x2_f16x2(c & 0xffffu), s2),
+                                      hmul2_u32(e4m3x2_f16x2(c >> 16), s2),
+                                      hmul2_u32(e4m3x2_f16x2(d & 0xffffu), s2),
+                                      hmul2_u32(e4m3x2_f16x2(d >> 16), s2));
+      *reinterpret_cast<uint4 *>(Rb + off[i][0]) = first;
+      *reinterpret_cast<uint4 *>(Rb + off[i][1]) = second;
     }
   }
 }
@@ -286,6 +323,16 @@ __device__ __forceinline__ void store_step(uint8_t *R, int pair, int ptid, int64
 __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms) {
   const int ptid = threadIdx.x - kProducerWarp0 * 32;
   const int lane = threadIdx.x & 31;
+  const int row0 = ptid >> 3, seg = ptid & 7;
+  const bool swap = (seg & 4) != 0;
+  uint32_t off[kItemsPerThread][2];   // R byte offsets of this thread's stores (pair 0)
+#pragma unroll
+  for (int i = 0; i < kItemsPerThread; ++i) {
+    const uint32_t row = (uint32_t)(row0 + i * kRowStride);
+    const uint32_t lo = sw128_offset(row, seg * 16, kRBlock), hi = sw128_offset(row, seg * 16 + 8, kRBlock);
+    off[i][0] = swap ? hi : lo;
+    off[i][1] = swap ? lo : hi;
+  }
   uint8_t *R = smem + kOffR;
   uint8_t *Qs = smem + kOffQ;
   const int *lists = reinterpret_cast<const int *>(smem + kOffList);
@@ -332,26 +379,35 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms) {
     const uint32_t ms_slot = qi & 1;
     if (!wait_bar(&ms->meta_full[ms_slot], (qi >> 1) & 1, ms)) break;
     const int *list = lists + ms_slot * kMaxSel;
-    Rows rows;
-    rows.nsel = ms->meta[ms_slot][0];
-    rows.nwin = ms->meta[ms_slot][1];
-    rows.win_first = ms->meta[ms_slot][2];
-    rows.err = 0;
+    Src S;
+    S.nsel = ms->meta[ms_slot][0];
+    S.nrows = S.nsel + ms->meta[ms_slot][1];
+    const int64_t win_first = ms->meta[ms_slot][2];
     const int64_t kv0 = ms->meta[ms_slot][3];
-    const int nch = n_chunks_of(rows.nsel + rows.nwin);
+    S.sel_b = P.kv_fp8 + kv0 * kDim + seg * 16;
+    S.sel_s = P.kv_scale + kv0 * (kDim / 32) + seg / 2;
+    S.win_b = P.swa_fp8 + win_first * kDim + seg * 16;
+    S.win_s = P.swa_scale + win_first * (kDim / 32) + seg / 2;
+    S.dummy_b = P.swa_fp8 + seg * 16;
+    S.dummy_s = P.swa_scale + seg / 2;
+    const int nch = n_chunks_of(S.nrows);
     // ---- chunks: 4 steps of 128 channels each; the loads of the next two
     // steps are in flight while a step waits for its buffer and is stored
     const int nsteps = nch * 4;
     Item b0[kItemsPerThread], b1[kItemsPerThread], b2[kItemsPerThread];
-    load_step(P, list, rows, kv0, 0, 0, ptid, b0);
-    if (nsteps > 1) load_step(P, list, rows, kv0, 0, 1, ptid, b1);
+    load_step(list, S, row0, 0, 0, b0);
+    if (nsteps > 1) load_step(list, S, row0, 0, 1, b1);
     bool ok = true;
     // one step: prefetch step st+2 into `pre`, then store step st from `use`
     auto step = [&](int st, Item(&use)[kItemsPerThread], Item(&pre)[kItemsPerThread]) -> bool {
       const int c = st >> 2, pair = st & 3;
-      if (st + 2 < nsteps) load_step(P, list, rows, kv0, (st + 2) >> 2, (st + 2) & 3, ptid, pre);
+      if (st + 2 < nsteps) load_step(list, S, row0, (st + 2) >> 2, (st + 2) & 3, pre);
       if (!wait_bar(&ms->r_empty[pair], ((g + c) & 1) ^ 1, ms)) return false;
-      store_step(R, pair, ptid, (int64_t)c * kRowsPerChunk, rows.nsel + rows.nwin, use);
+      const int64_t valid_rows = S.nrows - (int64_t)c * kRowsPerChunk;
+      if (valid_rows >= kRowsPerChunk)
+        store_step<false>(R, pair, swap, row0, off, valid_rows, use);
+      else
+        store_step<true>(R, pair, swap, row0, off, valid_rows, use);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ms->r_full[pair]);
