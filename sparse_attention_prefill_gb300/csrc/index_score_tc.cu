@@ -55,13 +55,16 @@ constexpr uint32_t kBBlock = kBRows * 128;             // 34 KB
 constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kOffA + kStages * kAStage;  // 128 KB
 constexpr uint32_t kOffMisc = kOffB + 2 * kBBlock;     // +68 KB
-constexpr uint32_t kSmemBytes = kOffMisc + 4096;
+constexpr uint32_t kOffCand = kOffMisc + 4096;         // candidate blocks of the chunk
+constexpr int kCandInts = 4096;                        // (16 KB; used when they fit)
+constexpr uint32_t kSmemBytes = kOffCand + kCandInts * 4;
 
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kDerrTimeout = 128;
 constexpr int kMaxQT = 32;
 
 struct RunInfo {
+  int64_t kv0;  // pool row of the request's entry 0
   int ql0, nq, req;
   int gather;   // 1: slots map through the query's candidate blocks
   int64_t len;  // longest row of the run
@@ -78,7 +81,9 @@ struct Misc {
   int64_t n_vis[kMaxQT];
   int nb[kMaxQT];            // pool mode: candidate blocks per query
   int ident[kMaxQT];         // pool mode: blocks are 0..nb-1
-  float w[256];              // head weights of the tile
+  int cand_smem;             // pool mode: the chunk's candidate blocks are in shared memory
+  int cand_span, b_lo;       //   as [query of the tile][block - b_lo]
+  alignas(16) float w[256];  // head weights of the tile
 };
 static_assert(sizeof(Misc) <= 4096, "misc");
 
@@ -150,20 +155,28 @@ struct Params {
   int32_t *d_err;
 };
 
+// candidate block bi of query q (q0 + ql): from the shared-memory copy of
+// this chunk's blocks when it fits, else from global memory
+__device__ __forceinline__ int64_t cand_block(const Params &P, const Misc *ms,
+                                              const int32_t *cand_s, int ql, int q, int bi) {
+  if (ms->cand_smem) return cand_s[ql * ms->cand_span + (bi - ms->b_lo)];
+  return P.cand[(int64_t)q * P.max_blocks + bi];
+}
+
 // key row of slot s of run `ri` (or -1 when the slot holds no visible entry):
 // full mode, entry s of the run's request; pool mode, the entry of the
 // query's candidate-block slot.
-__device__ __forceinline__ int64_t slot_row(const Params &P, const Misc *ms, int ri, int64_t s,
-                                            int q) {
+__device__ __forceinline__ int64_t slot_row(const Params &P, const Misc *ms,
+                                            const int32_t *cand_s, int ri, int64_t s, int q) {
   const RunInfo &ru = ms->runs[ri];
   if (s >= ru.len) return -1;
   int64_t j = s;
   if (!ru.gather && s >= ru.lim) return -1;
   if (ru.gather) {
-    j = (int64_t)P.cand[(int64_t)q * P.max_blocks + s / P.block] * P.block + s % P.block;
+    j = cand_block(P, ms, cand_s, ru.ql0, q, (int)(s / P.block)) * P.block + s % P.block;
     if (j >= ms->n_vis[ru.ql0]) return -1;
   }
-  return P.b.kv_start[ru.req] + j;
+  return ru.kv0 + j;
 }
 
 // ---------------------------------------------------------------------------
@@ -175,23 +188,24 @@ constexpr int kProdItems = (kKeyTile * 4 + kProdThreads - 1) / kProdThreads;
 struct KeyLoad {
   uint4 codes[kProdItems];
   float sc[kProdItems];
+  uint32_t valid;  // bit i: item i holds a visible key (else zeroed when stored)
 };
+static_assert(kProdItems * kProdThreads == kKeyTile * 4, "items cover the tile exactly");
 
-__device__ __forceinline__ void load_tile(const Params &P, const Misc *ms, int ri, int64_t kt,
-                                          int q, int ptid, KeyLoad &L) {
+// Every load is issued unconditionally (slots without a key read key row 0
+// and are zeroed when stored), so no load waits on another.
+__device__ __forceinline__ void load_tile(const Params &P, const Misc *ms, const int32_t *cand_s,
+                                          int ri, int64_t kt, int q, int ptid, KeyLoad &L) {
+  L.valid = 0;
 #pragma unroll
   for (int i = 0; i < kProdItems; ++i) {
     const int item = ptid + i * kProdThreads;
-    L.codes[i] = make_uint4(0, 0, 0, 0);
-    L.sc[i] = 0.f;
-    if (item < kKeyTile * 4) {
-      const int row = item >> 2, grp = item & 3;
-      const int64_t g = slot_row(P, ms, ri, kt * kKeyTile + row, q);
-      if (g >= 0) {
-        L.codes[i] = __ldg(reinterpret_cast<const uint4 *>(P.k_fp4 + g * 64) + grp);
-        L.sc[i] = __ldg(P.k_scale + g * 4 + grp);
-      }
-    }
+    const int row = item >> 2, grp = item & 3;
+    int64_t g = slot_row(P, ms, cand_s, ri, kt * kKeyTile + row, q);
+    L.valid |= (g >= 0 ? 1u : 0u) << i;
+    g = g >= 0 ? g : 0;
+    L.codes[i] = __ldg(reinterpret_cast<const uint4 *>(P.k_fp4 + g * 64) + grp);
+    L.sc[i] = __ldg(P.k_scale + g * 4 + grp);
   }
 }
 
@@ -217,7 +231,8 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
   int64_t kt = (int64_t)y * kTilesPerChunk - 1;
   if (!next_item(ms, y, ri, kt)) return;
   KeyLoad ka, kb;
-  load_tile(P, ms, ri, kt, q0 + ms->runs[ri].ql0, ptid, ka);
+  const int32_t *cand_s = reinterpret_cast<const int32_t *>(smem + kOffCand);
+  load_tile(P, ms, cand_s, ri, kt, q0 + ms->runs[ri].ql0, ptid, ka);
   bool more = true;
   // store the tile held in `use` after issuing the loads of the next tile
   // into `pre` (two fixed buffers: no register copy waits on pending loads)
@@ -225,21 +240,29 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
     int ri2 = ri;
     int64_t kt2 = kt;
     more = next_item(ms, y, ri2, kt2);
-    if (more) load_tile(P, ms, ri2, kt2, q0 + ms->runs[ri2].ql0, ptid, pre);
+    if (more) load_tile(P, ms, cand_s, ri2, kt2, q0 + ms->runs[ri2].ql0, ptid, pre);
     const uint32_t st = it % kStages;
     if (!wait_bar(&ms->a_empty[st], ((it / kStages) & 1) ^ 1, ms)) return false;
     uint8_t *A = smem + kOffA + st * kAStage;
 #pragma unroll
     for (int i = 0; i < kProdItems; ++i) {
       const int item = ptid + i * kProdThreads;
-      if (item < kKeyTile * 4) {
-        const int row = item >> 2, grp = item & 3;
-        if (use.sc[i] != 0.f && !mx_scale_ok(use.sc[i])) err |= CSA2_DERR_SCALE;
-        uint4 o[4];
-        dequant32(use.codes[i], use.sc[i], o);
+      const int row = item >> 2, grp = item & 3;
+      const bool v = (use.valid >> i) & 1u;
+      const float sc = v ? use.sc[i] : 0.f;
+      if (v && sc != 0.f && !mx_scale_ok(sc)) err |= CSA2_DERR_SCALE;
+      // groups 2-3 sit in the second 64-column block, whose 16-byte chunk
+      // positions repeat the first block's: they store their chunks rotated
+      // by two, so the 8 threads of a store phase hit 8 distinct positions
+      const bool rot = (grp & 2) != 0;
+      const uint4 c0 = v ? use.codes[i] : make_uint4(0, 0, 0, 0);
+      const uint4 cr = rot ? make_uint4(c0.z, c0.w, c0.x, c0.y) : c0;
+      uint4 o[4];
+      dequant32(cr, sc, o);
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4 *>(A + sw128_offset(row, grp * 32 + c * 8, kABlock)) = o[c];
+      for (int c = 0; c < 4; ++c) {
+        const int cc = rot ? (c + 2) & 3 : c;
+        *reinterpret_cast<uint4 *>(A + sw128_offset(row, grp * 32 + cc * 8, kABlock)) = o[c];
       }
     }
     fence_proxy_async_smem();
@@ -299,7 +322,8 @@ __device__ void mma_role(const Params &P, uint8_t *smem, Misc *ms, int y) {
 }
 
 template <int HI>
-__device__ void epilogue_role(const Params &P, Misc *ms, int q0, int y) {
+__device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, int y) {
+  const int32_t *cand_s = reinterpret_cast<const int32_t *>(smem + kOffCand);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sp = warp & 3, par = warp >> 2;
   const uint32_t tmem = ms->tmem_base;
@@ -317,36 +341,63 @@ __device__ void epilogue_role(const Params &P, Misc *ms, int q0, int y) {
       if (!(ok = wait_bar(&ms->d_full[db], (it >> 1) & 1, ms))) break;
       fence_after_sync();
       const int64_t s = kt * kKeyTile + 32 * sp + lane;
-      for (int qq = par; qq < ru.nq; qq += 2) {
-        const int ql = ru.ql0 + qq;
-        const int q = q0 + ql;
-        float acc = 0.f;
-#pragma unroll
-        for (int l = 0; l < NL; ++l) {
-          uint32_t v[32];
-          const uint32_t col = db * 256 + (uint32_t)(qq * HI + l * LW);
-          if constexpr (LW == 32) {
-            tmem_ld32x32b_x32(tmem + lane_addr + col, v);
-          } else if constexpr (LW == 16) {
-            tmem_ld32x32b_x16(tmem + lane_addr + col, v);
-          } else {
-            tmem_ld32x32b_x8(tmem + lane_addr + col, v);
-          }
-          tmem_wait_ld();
-#pragma unroll
-          for (int h = 0; h < LW; ++h)
-            acc = fmaf(ms->w[ql * HI + l * LW + h], fmaxf(__uint_as_float(v[h]), 0.f), acc);
-        }
+      // w . ReLU(D) over the HI head columns of query ql; store
+      auto finish = [&](int ql, float acc) {
         if (s < ms->row_len[ql]) {
           float outv = acc;
           if (P.cand) {
             const int64_t j =
-                ru.gather ? (int64_t)P.cand[(int64_t)q * P.max_blocks + s / P.block] * P.block +
+                ru.gather ? cand_block(P, ms, cand_s, ql, q0 + ql, (int)(s / P.block)) * P.block +
                                 s % P.block
                           : s;
             if (j >= ms->n_vis[ql]) outv = -INFINITY;
           }
-          P.scores[(int64_t)q * P.ld + s] = outv;
+          P.scores[(int64_t)(q0 + ql) * P.ld + s] = outv;
+        }
+      };
+      auto dot = [&](int ql, int h0, const uint32_t *v, int n, float acc) {
+        const float4 *w4 = reinterpret_cast<const float4 *>(ms->w + ql * HI + h0);
+#pragma unroll
+        for (int h = 0; h < n; h += 4) {
+          const float4 wv = w4[h / 4];
+          acc = fmaf(wv.x, fmaxf(__uint_as_float(v[h]), 0.f), acc);
+          acc = fmaf(wv.y, fmaxf(__uint_as_float(v[h + 1]), 0.f), acc);
+          acc = fmaf(wv.z, fmaxf(__uint_as_float(v[h + 2]), 0.f), acc);
+          acc = fmaf(wv.w, fmaxf(__uint_as_float(v[h + 3]), 0.f), acc);
+        }
+        return acc;
+      };
+      if constexpr (HI == 32) {
+        // two queries' columns in flight per TMEM wait
+        for (int qq = par; qq < ru.nq; qq += 4) {
+          const bool two = qq + 2 < ru.nq;   // uniform across the warp
+          uint32_t v0[32], v1[32];
+          const uint32_t col = db * 256 + (uint32_t)(qq * HI);
+          tmem_ld32x32b_x32(tmem + lane_addr + col, v0);
+          if (two) tmem_ld32x32b_x32(tmem + lane_addr + col + 2 * HI, v1);
+          tmem_wait_ld();
+          finish(ru.ql0 + qq, dot(ru.ql0 + qq, 0, v0, 32, 0.f));
+          if (two) finish(ru.ql0 + qq + 2, dot(ru.ql0 + qq + 2, 0, v1, 32, 0.f));
+        }
+      } else {
+        for (int qq = par; qq < ru.nq; qq += 2) {
+          const int ql = ru.ql0 + qq;
+          float acc = 0.f;
+#pragma unroll
+          for (int l = 0; l < NL; ++l) {
+            uint32_t v[32];
+            const uint32_t col = db * 256 + (uint32_t)(qq * HI + l * LW);
+            if constexpr (LW == 32) {
+              tmem_ld32x32b_x32(tmem + lane_addr + col, v);
+            } else if constexpr (LW == 16) {
+              tmem_ld32x32b_x16(tmem + lane_addr + col, v);
+            } else {
+              tmem_ld32x32b_x8(tmem + lane_addr + col, v);
+            }
+            tmem_wait_ld();
+            acc = dot(ql, l * LW, v, LW, acc);
+          }
+          finish(ql, acc);
         }
       }
       fence_before_sync();
@@ -388,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
   }
   if (threadIdx.x == 0) {
     ms->abort = 0;
+    ms->cand_smem = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&ms->a_full[i], kProdWarps);
       mbar_init(&ms->a_empty[i], 1);
@@ -402,10 +454,19 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
   __syncthreads();
   if (P.cand) {
     const int span = b_hi - b_lo;
+    const bool in_smem = QT * span <= kCandInts;
+    int32_t *cand_s = reinterpret_cast<int32_t *>(smem + kOffCand);
+    if (threadIdx.x == 0) {
+      ms->cand_smem = in_smem ? 1 : 0;
+      ms->cand_span = span;
+      ms->b_lo = b_lo;
+    }
     for (int i = threadIdx.x; i < QT * span; i += kThreads) {
       const int ql = i / span, bi = b_lo + i % span;
       const int q = q0 + ql;
-      if (q < P.b.num_q && P.cand[(int64_t)q * P.max_blocks + bi] < 0) atomicMin(&ms->nb[ql], bi);
+      const int32_t v = q < P.b.num_q ? P.cand[(int64_t)q * P.max_blocks + bi] : -1;
+      if (in_smem) cand_s[i] = v;
+      if (q < P.b.num_q && v < 0) atomicMin(&ms->nb[ql], bi);
     }
     __syncthreads();
   }
@@ -451,6 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
         if (len > ru.len) ru.len = len;
         if (lim > ru.lim) ru.lim = lim;
       } else {
+        ms->runs[nr].kv0 = P.b.kv_start[r];
         ms->runs[nr].ql0 = ql;
         ms->runs[nr].nq = 1;
         ms->runs[nr].req = r;
@@ -473,22 +535,40 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
   }
   // ---- query operand B: (query, head) rows x 128 f16, and head weights ----
   uint8_t *B = smem + kOffB;
-  for (int i = threadIdx.x; i < kBRows * 4; i += kThreads) {
-    const int row = i >> 2, grp = i & 3;
-    const int ql = row / HI, h = row % HI;
-    const int q = q0 + ql;
-    uint4 o[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
-                  make_uint4(0, 0, 0, 0)};
-    if (ql < QT && q < P.b.num_q) {
-      const int64_t base = (int64_t)q * HI + h;
-      const uint4 c = __ldg(reinterpret_cast<const uint4 *>(P.q_fp4 + base * 64) + grp);
-      const float sc = __ldg(P.q_scale + base * 4 + grp);
-      if (!mx_scale_ok(sc) && y == 0) err |= CSA2_DERR_SCALE;
-      dequant32(c, sc, o);
+  constexpr int kBItems = (kBRows * 4 + kThreads - 1) / kThreads;
+  {
+    // all loads first (rows past the tile read query row 0 and are zeroed)
+    uint4 c[kBItems];
+    float sc[kBItems];
+    uint32_t valid = 0;
+#pragma unroll
+    for (int k = 0; k < kBItems; ++k) {
+      const int i = threadIdx.x + k * kThreads;
+      const int row = (i >> 2) % kBRows, grp = i & 3;
+      const int ql = row / HI, h = row % HI;
+      const int q = q0 + ql;
+      const bool v = i < kBRows * 4 && ql < QT && q < P.b.num_q;
+      valid |= (v ? 1u : 0u) << k;
+      const int64_t base = v ? (int64_t)q * HI + h : 0;
+      c[k] = __ldg(reinterpret_cast<const uint4 *>(P.q_fp4 + base * 64) + grp);
+      sc[k] = __ldg(P.q_scale + base * 4 + grp);
     }
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      *reinterpret_cast<uint4 *>(B + sw128_offset(row, grp * 32 + c * 8, kBBlock)) = o[c];
+    for (int k = 0; k < kBItems; ++k) {
+      const int i = threadIdx.x + k * kThreads;
+      if (i < kBRows * 4) {
+        const int row = i >> 2, grp = i & 3;
+        uint4 o[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                      make_uint4(0, 0, 0, 0)};
+        if ((valid >> k) & 1u) {
+          if (!mx_scale_ok(sc[k]) && y == 0) err |= CSA2_DERR_SCALE;
+          dequant32(c[k], sc[k], o);
+        }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+          *reinterpret_cast<uint4 *>(B + sw128_offset(row, grp * 32 + cc * 8, kBBlock)) = o[cc];
+      }
+    }
   }
   for (int i = threadIdx.x; i < QT * HI; i += kThreads) {
     const int q = q0 + i / HI;
@@ -503,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
   __syncthreads();
   fence_after_sync();
   if (warp < kEpiWarps) {
-    epilogue_role<HI>(P, ms, q0, y);
+    epilogue_role<HI>(P, smem, ms, q0, y);
   } else if (warp == kMmaWarp) {
     mma_role(P, smem, ms, y);
   } else {
