@@ -155,28 +155,31 @@ struct Params {
   int32_t *d_err;
 };
 
-// candidate block bi of query q (q0 + ql): from the shared-memory copy of
-// this chunk's blocks when it fits, else from global memory
-__device__ __forceinline__ int64_t cand_block(const Params &P, const Misc *ms,
-                                              const int32_t *cand_s, int ql, int q, int bi) {
-  if (ms->cand_smem) return cand_s[ql * ms->cand_span + (bi - ms->b_lo)];
-  return P.cand[(int64_t)q * P.max_blocks + bi];
-}
-
-// key row of slot s of run `ri` (or -1 when the slot holds no visible entry):
-// full mode, entry s of the run's request; pool mode, the entry of the
-// query's candidate-block slot.
-__device__ __forceinline__ int64_t slot_row(const Params &P, const Misc *ms,
-                                            const int32_t *cand_s, int ri, int64_t s, int q) {
-  const RunInfo &ru = ms->runs[ri];
-  if (s >= ru.len) return -1;
-  int64_t j = s;
-  if (!ru.gather && s >= ru.lim) return -1;
-  if (ru.gather) {
-    j = cand_block(P, ms, cand_s, ru.ql0, q, (int)(s / P.block)) * P.block + s % P.block;
-    if (j >= ms->n_vis[ru.ql0]) return -1;
+// Candidate-block view of the tile, copied to registers once per tile: block
+// of slot s (a shift for power-of-two block sizes), and the entry it holds.
+struct CandView {
+  const int32_t *smem;   // [query of the tile][block - b_lo], or nullptr: global
+  const int32_t *glob;   // P.cand
+  int span, b_lo, max_blocks, block, shift;
+  __device__ __forceinline__ int blk(int s) const { return shift >= 0 ? s >> shift : s / block; }
+  __device__ __forceinline__ int64_t entry(int ql, int q, int s) const {
+    const int b = blk(s);
+    const int64_t c = smem ? smem[ql * span + (b - b_lo)] : glob[(int64_t)q * max_blocks + b];
+    return c * block + (s - b * block);
   }
-  return ru.kv0 + j;
+};
+
+__device__ __forceinline__ CandView cand_view(const Params &P, const Misc *ms,
+                                              const uint8_t *smem) {
+  CandView v;
+  v.smem = ms->cand_smem ? reinterpret_cast<const int32_t *>(smem + kOffCand) : nullptr;
+  v.glob = P.cand;
+  v.span = ms->cand_span;
+  v.b_lo = ms->b_lo;
+  v.max_blocks = P.max_blocks;
+  v.block = P.block;
+  v.shift = (P.block & (P.block - 1)) == 0 ? __ffs(P.block) - 1 : -1;
+  return v;
 }
 
 // ---------------------------------------------------------------------------
@@ -192,18 +195,31 @@ struct KeyLoad {
 };
 static_assert(kProdItems * kProdThreads == kKeyTile * 4, "items cover the tile exactly");
 
-// Every load is issued unconditionally (slots without a key read key row 0
-// and are zeroed when stored), so no load waits on another.
-__device__ __forceinline__ void load_tile(const Params &P, const Misc *ms, const int32_t *cand_s,
-                                          int ri, int64_t kt, int q, int ptid, KeyLoad &L) {
+// Key rows of tile kt of run ri: full mode, entry s of the run's request;
+// pool mode, the entry of the query's candidate-block slot s.  Slots past the
+// run's keys (or, in pool mode, holding no visible entry) read key row 0 and
+// are zeroed when stored: every load is issued unconditionally, so no load
+// waits on another.
+__device__ __forceinline__ void load_tile(const Params &P, const Misc *ms, const CandView &cv,
+                                          int ri, int64_t kt, int q0, int ptid, KeyLoad &L) {
+  const RunInfo ru = ms->runs[ri];
+  const int s0 = (int)kt * kKeyTile;
+  const int lim = (int)(ru.gather ? ru.len : min(ru.len, ru.lim));
+  const int64_t nvis = ms->n_vis[ru.ql0];
   L.valid = 0;
 #pragma unroll
   for (int i = 0; i < kProdItems; ++i) {
     const int item = ptid + i * kProdThreads;
     const int row = item >> 2, grp = item & 3;
-    int64_t g = slot_row(P, ms, cand_s, ri, kt * kKeyTile + row, q);
-    L.valid |= (g >= 0 ? 1u : 0u) << i;
-    g = g >= 0 ? g : 0;
+    const int s = s0 + row;
+    bool v = s < lim;
+    int64_t j = s;
+    if (ru.gather) {
+      j = v ? cv.entry(ru.ql0, q0 + ru.ql0, s) : 0;
+      v = v && j < nvis;
+    }
+    L.valid |= (v ? 1u : 0u) << i;
+    const int64_t g = v ? ru.kv0 + j : 0;
     L.codes[i] = __ldg(reinterpret_cast<const uint4 *>(P.k_fp4 + g * 64) + grp);
     L.sc[i] = __ldg(P.k_scale + g * 4 + grp);
   }
@@ -231,8 +247,8 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
   int64_t kt = (int64_t)y * kTilesPerChunk - 1;
   if (!next_item(ms, y, ri, kt)) return;
   KeyLoad ka, kb;
-  const int32_t *cand_s = reinterpret_cast<const int32_t *>(smem + kOffCand);
-  load_tile(P, ms, cand_s, ri, kt, q0 + ms->runs[ri].ql0, ptid, ka);
+  const CandView cv = cand_view(P, ms, smem);
+  load_tile(P, ms, cv, ri, kt, q0, ptid, ka);
   bool more = true;
   // store the tile held in `use` after issuing the loads of the next tile
   // into `pre` (two fixed buffers: no register copy waits on pending loads)
@@ -240,7 +256,7 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
     int ri2 = ri;
     int64_t kt2 = kt;
     more = next_item(ms, y, ri2, kt2);
-    if (more) load_tile(P, ms, cand_s, ri2, kt2, q0 + ms->runs[ri2].ql0, ptid, pre);
+    if (more) load_tile(P, ms, cv, ri2, kt2, q0, ptid, pre);
     const uint32_t st = it % kStages;
     if (!wait_bar(&ms->a_empty[st], ((it / kStages) & 1) ^ 1, ms)) return false;
     uint8_t *A = smem + kOffA + st * kAStage;
@@ -323,7 +339,7 @@ __device__ void mma_role(const Params &P, uint8_t *smem, Misc *ms, int y) {
 
 template <int HI>
 __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, int y) {
-  const int32_t *cand_s = reinterpret_cast<const int32_t *>(smem + kOffCand);
+  const CandView cv = cand_view(P, ms, smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sp = warp & 3, par = warp >> 2;
   const uint32_t tmem = ms->tmem_base;
@@ -340,16 +356,13 @@ __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
       const uint32_t db = it & 1;
       if (!(ok = wait_bar(&ms->d_full[db], (it >> 1) & 1, ms))) break;
       fence_after_sync();
-      const int64_t s = kt * kKeyTile + 32 * sp + lane;
+      const int s = (int)kt * kKeyTile + 32 * sp + lane;
       // w . ReLU(D) over the HI head columns of query ql; store
       auto finish = [&](int ql, float acc) {
         if (s < ms->row_len[ql]) {
           float outv = acc;
           if (P.cand) {
-            const int64_t j =
-                ru.gather ? cand_block(P, ms, cand_s, ql, q0 + ql, (int)(s / P.block)) * P.block +
-                                s % P.block
-                          : s;
+            const int64_t j = ru.gather ? cv.entry(ql, q0 + ql, s) : s;
             if (j >= ms->n_vis[ql]) outv = -INFINITY;
           }
           P.scores[(int64_t)(q0 + ql) * P.ld + s] = outv;
