@@ -22,10 +22,10 @@
 // has its own slot list and is its own run, except that identity pools
 // (blocks 0, 1, ..., nb-1: nothing excluded, the case when every reachable
 // position fits the pool budget) map slot s to entry s and merge like full
-// mode.  Roles (13 warps):
+// mode.  Roles (16 warps):
 //   warps 0-7   epilogue (warp w: TMEM lanes 32*(w%4).., queries of parity w/4)
 //   warp 8      TMEM allocation; lane 0 issues the MMAs
-//   warps 9-12  producers: key gather + E2M1 -> f16 into a 4-stage ring, one
+//   warps 9-15  producers: key gather + E2M1 -> f16 into a 4-stage ring, one
 //               key tile of loads in flight ahead of the ring
 // Waits are time-bounded (CSA2_DERR_TIMEOUT on expiry).
 #include "common.cuh"
@@ -43,8 +43,8 @@ constexpr int kStages = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kMmaWarp = 8;
 constexpr int kProdWarp0 = 9;
-constexpr int kProdWarps = 4;
-constexpr int kWarps = 13;
+constexpr int kProdWarps = 7;
+constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kProdThreads = kProdWarps * 32;
 constexpr int kBRows = 256 + 16;       // (query, head) rows + padding for N rounding
@@ -193,7 +193,7 @@ struct KeyLoad {
   float sc[kProdItems];
   uint32_t valid;  // bit i: item i holds a visible key (else zeroed when stored)
 };
-static_assert(kProdItems * kProdThreads == kKeyTile * 4, "items cover the tile exactly");
+static_assert(kProdThreads % 4 == 0, "a thread's items share one 32-dim group");
 
 // Key rows of tile kt of run ri: full mode, entry s of the run's request;
 // pool mode, the entry of the query's candidate-block slot s.  Slots past the
@@ -212,7 +212,7 @@ __device__ __forceinline__ void load_tile(const Params &P, const Misc *ms, const
     const int item = ptid + i * kProdThreads;
     const int row = item >> 2, grp = item & 3;
     const int s = s0 + row;
-    bool v = s < lim;
+    bool v = item < kKeyTile * 4 && s < lim;
     int64_t j = s;
     if (ru.gather) {
       j = v ? cv.entry(ru.ql0, q0 + ru.ql0, s) : 0;
@@ -263,6 +263,7 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
 #pragma unroll
     for (int i = 0; i < kProdItems; ++i) {
       const int item = ptid + i * kProdThreads;
+      if (item >= kKeyTile * 4) break;
       const int row = item >> 2, grp = item & 3;
       const bool v = (use.valid >> i) & 1u;
       const float sc = v ? use.sc[i] : 0.f;
