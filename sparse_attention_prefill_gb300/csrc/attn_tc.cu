@@ -210,11 +210,15 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, __half2 s) {
   return *reinterpret_cast<uint32_t *>(&x);
 }
 
-__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two) {
-  uint32_t h2;
-  const uint16_t v = (uint16_t)two;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
-  return h2;
+// four E4M3 codes -> two f16x2 (low code pair -> lo); the halves are taken
+// apart by a vector move, not by shifts
+__device__ __forceinline__ void e4m3x4_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  asm("{ .reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 // One pipeline step: channels [128*pair, 128*pair+128) of the 128 rows of a
@@ -306,14 +310,15 @@ __device__ __forceinline__ void store_step(uint8_t *R, int pair, bool swap, int 
       const __half2 s2 = __float2half2_rn(sc);
       const uint32_t a = swap ? cd.z : cd.x, b = swap ? cd.w : cd.y;
       const uint32_t c = swap ? cd.x : cd.z, d = swap ? cd.y : cd.w;
-      const uint4 first = make_uint4(hmul2_u32(e4m3x2_f16x2(a & 0xffffu), s2),
-                                     hmul2_u32(e4m3x2_f16x2(a >> 16), s2),
-                                     hmul2_u32(e4m3x2_f16x2(b & 0xffffu), s2),
-                                     hmul2_u32(e4m3x2_f16x2(b >> 16), s2));
-      const uint4 second = make_uint4(hmul2_u32(e4m3x2_f16x2(c & 0xffffu), s2),
-                                      hmul2_u32(e4m3x2_f16x2(c >> 16), s2),
-                                      hmul2_u32(e4m3x2_f16x2(d & 0xffffu), s2),
-                                      hmul2_u32(e4m3x2_f16x2(d >> 16), s2));
+      uint32_t h[8];
+      e4m3x4_f16x4(a, h[0], h[1]);
+      e4m3x4_f16x4(b, h[2], h[3]);
+      e4m3x4_f16x4(c, h[4], h[5]);
+      e4m3x4_f16x4(d, h[6], h[7]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) h[j] = hmul2_u32(h[j], s2);
+      const uint4 first = make_uint4(h[0], h[1], h[2], h[3]);
+      const uint4 second = make_uint4(h[4], h[5], h[6], h[7]);
       *reinterpret_cast<uint4 *>(Rb + off[i][0]) = first;
       *reinterpret_cast<uint4 *>(Rb + off[i][1]) = second;
     }

@@ -83,7 +83,7 @@ struct Misc {
   int ident[kMaxQT];         // pool mode: blocks are 0..nb-1
   int cand_smem;             // pool mode: the chunk's candidate blocks are in shared memory
   int cand_span, b_lo;       //   as [query of the tile][block - b_lo]
-  alignas(16) float w[256];  // head weights of the tile
+  alignas(16) float w[256];  // head weights of the tile, halved
 };
 static_assert(sizeof(Misc) <= 4096, "misc");
 
@@ -112,18 +112,23 @@ __device__ __forceinline__ bool mx_scale_ok(float s) {
   return (u & 0x807fffffu) == 0 && e >= -23 && e <= 12;
 }
 
-// two E2M1 codes (one byte, element 2i in the low nibble) -> f16x2
-__device__ __forceinline__ uint32_t e2m1x2_f16x2(uint32_t byte) {
-  uint32_t r;
-  const uint16_t v = (uint16_t)byte;
-  asm("{ .reg .b8 t; cvt.u8.u16 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(r) : "h"(v));
-  return r;
-}
-
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, __half2 s) {
   __half2 x = *reinterpret_cast<__half2 *>(&a);
   x = __hmul2(x, s);
   return *reinterpret_cast<uint32_t *>(&x);
+}
+
+// four bytes of E2M1 code pairs -> four f16x2 (byte b -> h[b]; low nibble in
+// the low half); the bytes are taken apart by a vector move, not by shifts
+__device__ __forceinline__ void e2m1x8_f16x8(uint32_t w, uint32_t (&h)[4]) {
+  asm("{ .reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
 }
 
 // 32 E2M1 codes (16 bytes) times a power-of-two scale -> 32 f16 (4 x uint4)
@@ -133,8 +138,9 @@ __device__ __forceinline__ void dequant32(const uint4 c, float scale, uint4 (&o)
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     uint32_t h[4];
+    e2m1x8_f16x8(w[i], h);
 #pragma unroll
-    for (int b = 0; b < 4; ++b) h[b] = hmul2_u32(e2m1x2_f16x2((w[i] >> (8 * b)) & 0xffu), s2);
+    for (int b = 0; b < 4; ++b) h[b] = hmul2_u32(h[b], s2);
     o[i] = make_uint4(h[0], h[1], h[2], h[3]);
   }
 }
@@ -369,17 +375,26 @@ __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
           P.scores[(int64_t)(q0 + ql) * P.ld + s] = outv;
         }
       };
+      // w * ReLU(x) as (w/2) * (x + |x|): the same value (halving and
+      // doubling are exact), on the FMA pipe instead of a min/max on the ALU
+      // pipe.  ms->w holds w/2.
+      auto relu2 = [](uint32_t x) {
+        const float f = __uint_as_float(x);
+        return f + fabsf(f);
+      };
+      // four partial sums (heads h mod 4): independent FMA chains
       auto dot = [&](int ql, int h0, const uint32_t *v, int n, float acc) {
         const float4 *w4 = reinterpret_cast<const float4 *>(ms->w + ql * HI + h0);
+        float a0 = acc, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
         for (int h = 0; h < n; h += 4) {
           const float4 wv = w4[h / 4];
-          acc = fmaf(wv.x, fmaxf(__uint_as_float(v[h]), 0.f), acc);
-          acc = fmaf(wv.y, fmaxf(__uint_as_float(v[h + 1]), 0.f), acc);
-          acc = fmaf(wv.z, fmaxf(__uint_as_float(v[h + 2]), 0.f), acc);
-          acc = fmaf(wv.w, fmaxf(__uint_as_float(v[h + 3]), 0.f), acc);
+          a0 = fmaf(wv.x, relu2(v[h]), a0);
+          a1 = fmaf(wv.y, relu2(v[h + 1]), a1);
+          a2 = fmaf(wv.z, relu2(v[h + 2]), a2);
+          a3 = fmaf(wv.w, relu2(v[h + 3]), a3);
         }
-        return acc;
+        return (a0 + a1) + (a2 + a3);
       };
       if constexpr (HI == 32) {
         // two queries' columns in flight per TMEM wait
@@ -586,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
   }
   for (int i = threadIdx.x; i < QT * HI; i += kThreads) {
     const int q = q0 + i / HI;
-    ms->w[i] = (q < P.b.num_q) ? (P.head_w ? P.head_w[(int64_t)q * HI + i % HI] : 1.f) : 0.f;
+    ms->w[i] = (q < P.b.num_q) ? 0.5f * (P.head_w ? P.head_w[(int64_t)q * HI + i % HI] : 1.f) : 0.f;
   }
   fence_proxy_async_smem();
   if (warp == kMmaWarp) {
