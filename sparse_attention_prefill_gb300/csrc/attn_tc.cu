@@ -439,6 +439,16 @@ __device__ void mma_role(const Params &P, uint8_t *smem, Misc *ms) {
                  p0 = smem_u32(smem + kOffP);
   const uint32_t id_s = make_idesc_f16(128, kHeadsPad, false, false);
   const uint32_t id_o = make_idesc_f16(128, kHeadsPad, true, true);
+  // base descriptors; every MMA's operand descriptor is one of these plus a
+  // compile-time offset
+  const uint64_t d_rk = make_desc_sw128(r0, 16, 1024);        // R, K-major (S)
+  const uint64_t d_q = make_desc_sw128(q0, 16, 1024);         // Q, K-major (S)
+  const uint64_t d_rm = make_desc_sw128(r0, kRBlock, 1024);   // R^T, MN-major (O)
+  const uint64_t d_p = make_desc_sw128(p0, kRBlock, 1024);    // P^T, MN-major (O)
+  const uint32_t rk_lo = (uint32_t)d_rk, rk_hi = (uint32_t)(d_rk >> 32);
+  const uint32_t q_lo = (uint32_t)d_q, q_hi = (uint32_t)(d_q >> 32);
+  const uint32_t rm_lo = (uint32_t)d_rm, rm_hi = (uint32_t)(d_rm >> 32);
+  const uint32_t p_lo = (uint32_t)d_p, p_hi = (uint32_t)(d_p >> 32);
   uint32_t g = 0, qi = 0;
   int ok = 1;
   for (int q = blockIdx.x; q < P.b.num_q && lane == 0; q += gridDim.x, ++qi) {
@@ -456,12 +466,14 @@ __device__ void mma_role(const Params &P, uint8_t *smem, Misc *ms) {
           ok = wait_bar(&ms->r_full[pair], g & 1, ms);
           if (!ok) break;
           fence_after_sync();
+          const uint32_t a_p = rk_lo + ((pair * 2 * kRBlock) >> 4);
+          const uint32_t b_p = q_lo + ((pair * 2 * kQBlock) >> 4);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const int blk = pair * 2 + (kk >> 2);
-            const uint64_t a = make_desc_sw128(r0 + blk * kRBlock + (kk & 3) * 32, 16, 1024);
-            const uint64_t bq = make_desc_sw128(q0 + blk * kQBlock + (kk & 3) * 32, 16, 1024);
-            mma_f16(s_tmem, a, bq, id_s, (pair > 0 || kk > 0) ? 1u : 0u);
+            const uint32_t oa = ((kk >> 2) * kRBlock + (kk & 3) * 32) >> 4;
+            const uint32_t ob = ((kk >> 2) * kQBlock + (kk & 3) * 32) >> 4;
+            mma_f16_split(s_tmem, a_p + oa, rk_hi, b_p + ob, q_hi, id_s,
+                          (pair > 0 || kk > 0) ? 1u : 0u);
           }
         }
         if (!ok) break;
@@ -472,12 +484,13 @@ __device__ void mma_role(const Params &P, uint8_t *smem, Misc *ms) {
         if (ok && c == 0) ok = wait_bar(&ms->o_empty, (qi & 1) ^ 1, ms);
         if (!ok) break;
         fence_after_sync();
+#pragma unroll
         for (int t = 0; t < 4; ++t) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t a = make_desc_sw128(r0 + t * 2 * kRBlock + ks * 2048, kRBlock, 1024);
-            const uint64_t bp = make_desc_sw128(p0 + ks * 2048, kRBlock, 1024);
-            mma_f16(tmem + kColO + t * 64, a, bp, id_o, (c > 0 || ks > 0) ? 1u : 0u);
+            mma_f16_split(tmem + kColO + t * 64, rm_lo + ((t * 2 * kRBlock + ks * 2048) >> 4),
+                          rm_hi, p_lo + ((ks * 2048) >> 4), p_hi, id_o,
+                          (c > 0 || ks > 0) ? 1u : 0u);
           }
           mma_commit(&ms->r_empty[t]);
         }

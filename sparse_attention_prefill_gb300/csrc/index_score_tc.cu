@@ -325,12 +325,12 @@ __device__ void mma_role(const Params &P, uint8_t *smem, Misc *ms, int y) {
         if (!(ok = wait_bar(&ms->d_empty[db], ((it >> 1) & 1) ^ 1, ms))) break;
         fence_after_sync();
         const uint32_t a0 = smem_u32(smem + kOffA + st * kAStage);
+        const uint64_t da = make_desc_sw128(a0, 16, 1024);
+        const uint64_t dbq = make_desc_sw128(b0 + brow, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a = make_desc_sw128(a0 + (kk >> 2) * kABlock + (kk & 3) * 32, 16, 1024);
-          const uint64_t bq = make_desc_sw128(b0 + (kk >> 2) * kBBlock + brow + (kk & 3) * 32, 16,
-                                              1024);
-          mma_f16(tmem + db * 256, a, bq, idesc, kk > 0 ? 1u : 0u);
+          mma_f16(tmem + db * 256, desc_add(da, (kk >> 2) * kABlock + (kk & 3) * 32),
+                  desc_add(dbq, (kk >> 2) * kBBlock + (kk & 3) * 32), idesc, kk > 0 ? 1u : 0u);
         }
         mma_commit(&ms->a_empty[st]);
         mma_commit(&ms->d_full[db]);

@@ -51,6 +51,15 @@ __device__ __forceinline__ uint64_t make_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// Descriptor of the same operand layout at a shared-memory address `byte_off`
+// bytes further on: the start-address field holds address >> 4 in 14 bits and
+// shared-memory addresses stay below 256 KB, so the sum never carries out of
+// the field.  Costs one add instead of rebuilding the descriptor (the MMA
+// issuing thread is otherwise the bottleneck for narrow MMAs).
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t byte_off) {
+  return desc + (uint64_t)(byte_off >> 4);
+}
+
 // Instruction descriptor for kind::f16 with f16 A/B, f32 accumulate.
 //   [4,6) D format (1 = f32)  [7,10) A format (0 = f16)  [10,13) B format
 //   [15] A MN-major  [16] B MN-major  [17,23) N >> 3  [24,29) M >> 4
@@ -87,6 +96,23 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The same MMA with each operand descriptor given as (low, high) words.  In a
+// sequence over one operand layout the high words never change and the low
+// words differ by compile-time offsets, so each MMA costs one 32-bit add per
+// operand: narrow MMAs are otherwise limited by the issuing thread.
+__device__ __forceinline__ void mma_f16_split(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                              uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 a, b;\n\t"
+      "mov.b64 a, {%1, %2};\n\t"
+      "mov.b64 b, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
