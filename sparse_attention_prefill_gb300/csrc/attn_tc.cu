@@ -9,23 +9,31 @@
 //   O[q,h]  = softmax_i(sm_scale <Q[q,h], row_i>) . rows
 //
 // Formulation.  A query has H <= 64 heads (zero-padded to 64) and up to
-// k + window rows of 512 channels.  Rows are processed in chunks of 128 and
-// every product is written transposed so that the MMA M dimension is 128:
-//   S^T[r, h] = sum_d R[r, d] Q[h, d]          (M = 128 rows,  N = 64, K = 512)
-//   O^T[d, h] += sum_r R[r, d] P[r, h]         (M = 128 chans, N = 64, K = 128; 4 tiles)
-// One f16 copy of the chunk R (SW128 layout, 8 column blocks of 64 channels)
-// is the K-major A operand of the first product and the MN-major A operand of
-// the second.  S^T is double-buffered in TMEM (2 x 64 columns), O^T occupies
-// 4 x 64 columns.  The softmax runs online with a lazily updated reference
-// maximum per head: it is only moved (and O^T and the row sums rescaled) when
+// k + window rows of 512 channels, processed in chunks of 64 rows.  Both
+// products are written transposed:
+//   S^T[r, h] = sum_d R[r, d] Q[h, d]          (M = 64 rows,   N = 64, K = 512)
+//   O^T[d, h] += sum_r R[r, d] P[r, h]         (M = 128 chans, N = 64, K = 64; 4 tiles)
+// One f16 copy of the chunk (SW128 layout, 8 column blocks of 64 channels) is
+// the K-major A operand of the first product and the MN-major A operand of
+// the second.  Chunks are double-buffered in shared memory (R and P), S^T in
+// TMEM (2 x 64 columns; an M = 64 accumulator fills lanes 0-15 of each 32-lane
+// sub-partition) and O^T takes 4 x 64 TMEM columns.  The MMA issuer runs S^T
+// one chunk ahead of O^T, so gathering, softmax and both products of
+// neighbouring chunks overlap.  The softmax keeps a lazily moved reference
+// maximum per head: it moves (and O^T and the row sums are rescaled) only when
 // a logit exceeds it by more than 2^8, so P <= 256 always fits f16.
 //
 // Roles (16 warps, one CTA per SM, persistent over queries):
-//   warps 0-7   softmax + epilogue; warp w owns TMEM lanes 32*(w%4).. (rows of
-//               S^T / channels of O^T) and heads 32*(w/4) .. +31
-//   warp 8      TMEM allocation; lane 0 issues every MMA and commit
-//   warps 9-15  producers: Q (bf16 -> f16), row gather + E4M3 -> f16 dequant,
-//               in 4 pipeline steps of 128 channels per chunk
+//   warps 0-7   softmax + epilogue; warp w reads TMEM sub-partition w%4 and
+//               heads 32*(w/4) .. +31 (rows of S^T, channels of O^T); warp 0
+//               also builds the next query's row list one query ahead
+//   warp 8      TMEM allocation; lane 0 issues the S^T MMAs
+//   warp 9      lane 0 issues the O^T MMAs (the two products of neighbouring
+//               chunks are issued independently, so neither waits behind the
+//               other in one issuing thread)
+//   warps 10-15 producers: Q (bf16 -> f16 via cp.async, converted in place),
+//               row gather + E4M3 -> f16 dequant in steps of 32 rows, loads
+//               issued one step ahead
 // Every wait is bounded (about two seconds); on expiry the kernel raises
 // CSA2_DERR_TIMEOUT, drains and returns.
 #include "common.cuh"
@@ -38,43 +46,46 @@ namespace {
 using namespace tc;
 
 constexpr int kDim = 512;
-constexpr int kRowsPerChunk = 128;
+constexpr int kChunk = 64;            // rows per chunk (S^T MMA M)
+constexpr int kStepRows = 32;         // rows per producer step
 constexpr int kHeadsPad = 64;
 constexpr int kSoftmaxWarps = 8;
-constexpr int kMmaWarp = 8;
-constexpr int kProducerWarp0 = 9;
-constexpr int kProducerWarps = 7;
+constexpr int kMmaWarp = 8;            // TMEM allocation; lane 0 issues S^T
+constexpr int kOWarp = 9;              // lane 0 issues O^T
+constexpr int kProducerWarp0 = 10;
+constexpr int kProducerWarps = 6;
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kProducerThreads = kProducerWarps * 32;
 constexpr int kMaxSel = 2048;
 
 // shared-memory map (bytes)
-constexpr uint32_t kOffR = 0;           // 8 blocks x [128 rows x 128 B]  (128 KB)
-constexpr uint32_t kRBlock = 16384;
-constexpr uint32_t kOffQ = 131072;      // 8 blocks x [64 heads x 128 B]  (64 KB)
-constexpr uint32_t kQBlock = 8192;
-constexpr uint32_t kOffP = 196608;      // [128 rows x 64 heads] f16       (16 KB)
-constexpr uint32_t kOffList = 212992;   // 2 x int32 [kMaxSel]             (16 KB)
-constexpr uint32_t kOffMisc = 229376;
+constexpr uint32_t kRBlock = kChunk * 128;       // 8 KB: 64 rows x 64 channels f16
+constexpr uint32_t kRBuf = 8 * kRBlock;          // 64 KB per chunk buffer
+constexpr uint32_t kOffR = 0;                    // 2 chunk buffers (128 KB)
+constexpr uint32_t kQBlock = kHeadsPad * 128;    // 8 KB
+constexpr uint32_t kOffQ = 2 * kRBuf;            // 64 KB
+constexpr uint32_t kPBuf = kChunk * 128;         // 8 KB: 64 rows x 64 heads f16
+constexpr uint32_t kOffP = kOffQ + 8 * kQBlock;  // 2 x 8 KB
+constexpr uint32_t kOffList = kOffP + 2 * kPBuf; // 2 x int32 [kMaxSel] (16 KB)
+constexpr uint32_t kOffMisc = kOffList + 2 * kMaxSel * 4;
 constexpr uint32_t kSmemBytes = kOffMisc + 2048;
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;           // 2 x 64
+constexpr uint32_t kColS = 0;           // 2 x 64 (M = 64 layout)
 constexpr uint32_t kColO = 128;         // 4 x 64
 
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kDerrTimeout = 128;
 
 struct Misc {
-  uint64_t q_full, q_empty, s_full[2], s_empty[2], p_full, p_empty, o_full, o_empty, done;
-  uint64_t r_full[4], r_empty[4];
-  uint64_t sm_grp;          // group sync of the softmax warps
+  uint64_t q_full, q_empty, o_full, o_empty, done, done_o, sm_grp;
+  uint64_t r_full[2], r_empty[2], s_full[2], s_empty[2], p_full[2], p_empty[2];
   uint64_t meta_full[2];
-  int64_t meta[2][4];       // per query (ring of 2): selected rows, window rows, first SWA
-                            // row, pool row of the request's entry 0
+  int64_t meta[2][4];   // per query (ring of 2): selected rows, window rows, first SWA
+                        // row, pool row of the request's entry 0
   uint32_t tmem_base;
   int abort;
   int votes[2][8];      // softmax warps: "a logit exceeded the reference", by chunk parity
@@ -173,7 +184,7 @@ __device__ Rows query_rows(const Batch &b, int q, const int32_t *__restrict__ id
 }
 
 __device__ __forceinline__ int n_chunks_of(int64_t nrows) {
-  const int64_t c = (nrows + kRowsPerChunk - 1) / kRowsPerChunk;
+  const int64_t c = (nrows + kChunk - 1) / kChunk;
   return c > 0 ? (int)c : 1;
 }
 
@@ -221,14 +232,14 @@ __device__ __forceinline__ void e4m3x4_f16x4(uint32_t w, uint32_t &lo, uint32_t 
       : "r"(w));
 }
 
-// One pipeline step: channels [128*pair, 128*pair+128) of the 128 rows of a
-// chunk, as 1024 items of 16 channels.  Item ptid + 28*8*i of a producer
-// thread is segment ptid%8 (16 channels) of row ptid/8 + 28i: the segment is
-// the same for every item and step of a thread, so the per-thread address
-// parts are fixed once per query and only the row changes per item.
-constexpr int kRowStride = kProducerThreads / 8;   // rows between a thread's items
-constexpr int kItemsPerThread = (kRowsPerChunk + kRowStride - 1) / kRowStride;
-static_assert(kProducerThreads % 8 == 0, "segment fixed per thread");
+// One producer step: 32 rows x 512 channels, as 1024 items of 16 channels.
+// Producer thread p handles segment p%32 (channels 16*(p%32) ..) of rows
+// p/32 + 7i: the segment is the same for every item and step of a thread (a
+// warp covers whole 512-byte rows), so the per-thread address parts are fixed
+// once per query and only the row changes per item.
+constexpr int kRowStride = kProducerThreads / 32;   // rows between a thread's items
+constexpr int kItemsPerThread = (kStepRows + kRowStride - 1) / kRowStride;
+static_assert(kProducerThreads % 32 == 0, "segment fixed per thread");
 
 // Per-thread, per-query source bases (segment offset folded in).
 struct Src {
@@ -241,32 +252,31 @@ struct Src {
   int64_t nsel, nrows;
 };
 
-__device__ __forceinline__ void load_step(const int *list, const Src &S, int row0, int chunk,
-                                          int pair, Item (&it)[kItemsPerThread]) {
-  const int64_t r0 = (int64_t)chunk * kRowsPerChunk;
-  const int cb = pair * 128, sb = pair * 4;
-  if (r0 + kRowsPerChunk <= S.nsel) {          // every row selected
+__device__ __forceinline__ void load_step(const int *list, const Src &S, int row0, int step,
+                                          Item (&it)[kItemsPerThread]) {
+  const int64_t r0 = (int64_t)step * kStepRows;
+  if (r0 + kStepRows <= S.nsel) {            // every row selected
 #pragma unroll
     for (int i = 0; i < kItemsPerThread; ++i) {
-      if (row0 + i * kRowStride < kRowsPerChunk) {
+      if (row0 + i * kRowStride < kStepRows) {
         const int64_t j = list[r0 + row0 + i * kRowStride];
-        it[i].codes = __ldg(reinterpret_cast<const uint4 *>(S.sel_b + j * kDim + cb));
-        it[i].scale = __ldg(S.sel_s + j * (kDim / 32) + sb);
+        it[i].codes = __ldg(reinterpret_cast<const uint4 *>(S.sel_b + j * kDim));
+        it[i].scale = __ldg(S.sel_s + j * (kDim / 32));
       }
     }
-  } else if (r0 >= S.nsel && r0 + kRowsPerChunk <= S.nrows) {   // every row in the window
+  } else if (r0 >= S.nsel && r0 + kStepRows <= S.nrows) {   // every row in the window
 #pragma unroll
     for (int i = 0; i < kItemsPerThread; ++i) {
-      if (row0 + i * kRowStride < kRowsPerChunk) {
+      if (row0 + i * kRowStride < kStepRows) {
         const int64_t w = r0 + row0 + i * kRowStride - S.nsel;
-        it[i].codes = __ldg(reinterpret_cast<const uint4 *>(S.win_b + w * kDim + cb));
-        it[i].scale = __ldg(S.win_s + w * (kDim / 32) + sb);
+        it[i].codes = __ldg(reinterpret_cast<const uint4 *>(S.win_b + w * kDim));
+        it[i].scale = __ldg(S.win_s + w * (kDim / 32));
       }
     }
-  } else {                                     // boundary or last chunk
+  } else {                                     // boundary or last step
 #pragma unroll
     for (int i = 0; i < kItemsPerThread; ++i) {
-      if (row0 + i * kRowStride < kRowsPerChunk) {
+      if (row0 + i * kRowStride < kStepRows) {
         const int64_t ri = r0 + row0 + i * kRowStride;
         const uint8_t *b;
         const float *sc;
@@ -281,26 +291,28 @@ __device__ __forceinline__ void load_step(const int *list, const Src &S, int row
           b = S.dummy_b;
           sc = S.dummy_s;
         }
-        it[i].codes = __ldg(reinterpret_cast<const uint4 *>(b + cb));
-        it[i].scale = __ldg(sc + sb);
+        it[i].codes = __ldg(reinterpret_cast<const uint4 *>(b));
+        it[i].scale = __ldg(sc);
       }
     }
   }
 }
 
-// Dequantise a step into R.  off[i][0..1]: byte offsets (pair 0) of the two
-// 16-byte stores of item i.  The 8 threads of a store phase cover one row's 8
-// segments; segments 0-3 and 4-7 fall in two column blocks whose 16-byte
-// chunks share banks, so threads of segments 4-7 store their upper half
-// first: every phase then touches 8 distinct chunk positions.
+// Dequantise a step into rows 32*half .. +31 of the chunk buffer R.
+// off[i][0..1]: byte offsets (half 0) of the two 16-byte stores of item i;
+// half 1 is 32 rows (4096 bytes) further.  The 8 threads of a store phase
+// cover 8 consecutive segments: segments 4-7 of each group sit in the next
+// column block, whose 16-byte chunk positions repeat the first block's, so
+// they store their upper half first and every phase touches 8 distinct
+// positions.  Rows at or past `valid_rows` (step-relative) are written as zeros.
 template <bool kMasked>
-__device__ __forceinline__ void store_step(uint8_t *R, int pair, bool swap, int row0,
+__device__ __forceinline__ void store_step(uint8_t *R, int half, bool swap, int row0,
                                            const uint32_t (&off)[kItemsPerThread][2],
                                            int64_t valid_rows, const Item (&it)[kItemsPerThread]) {
-  uint8_t *Rb = R + pair * 2 * kRBlock;
+  uint8_t *Rb = R + half * (kStepRows / 8) * 1024;
 #pragma unroll
   for (int i = 0; i < kItemsPerThread; ++i) {
-    if (row0 + i * kRowStride < kRowsPerChunk) {
+    if (row0 + i * kRowStride < kStepRows) {
       uint4 cd = it[i].codes;
       float sc = it[i].scale;
       if (kMasked && row0 + i * kRowStride >= valid_rows) {
@@ -317,10 +329,8 @@ __device__ __forceinline__ void store_step(uint8_t *R, int pair, bool swap, int 
       e4m3x4_f16x4(d, h[6], h[7]);
 #pragma unroll
       for (int j = 0; j < 8; ++j) h[j] = hmul2_u32(h[j], s2);
-      const uint4 first = make_uint4(h[0], h[1], h[2], h[3]);
-      const uint4 second = make_uint4(h[4], h[5], h[6], h[7]);
-      *reinterpret_cast<uint4 *>(Rb + off[i][0]) = first;
-      *reinterpret_cast<uint4 *>(Rb + off[i][1]) = second;
+      *reinterpret_cast<uint4 *>(Rb + off[i][0]) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4 *>(Rb + off[i][1]) = make_uint4(h[4], h[5], h[6], h[7]);
     }
   }
 }
@@ -328,17 +338,17 @@ __device__ __forceinline__ void store_step(uint8_t *R, int pair, bool swap, int 
 __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms) {
   const int ptid = threadIdx.x - kProducerWarp0 * 32;
   const int lane = threadIdx.x & 31;
-  const int row0 = ptid >> 3, seg = ptid & 7;
+  const int row0 = ptid >> 5, seg = lane;
   const bool swap = (seg & 4) != 0;
-  uint32_t off[kItemsPerThread][2];   // R byte offsets of this thread's stores (pair 0)
+  uint32_t off[kItemsPerThread][2];   // R byte offsets of this thread's stores (half 0)
 #pragma unroll
   for (int i = 0; i < kItemsPerThread; ++i) {
-    const uint32_t row = (uint32_t)(row0 + i * kRowStride);
-    const uint32_t lo = sw128_offset(row, seg * 16, kRBlock), hi = sw128_offset(row, seg * 16 + 8, kRBlock);
+    const uint32_t row = (uint32_t)(row0 + i * kRowStride) & (kStepRows - 1);
+    const uint32_t lo = sw128_offset(row, seg * 16, kRBlock);
+    const uint32_t hi = sw128_offset(row, seg * 16 + 8, kRBlock);
     off[i][0] = swap ? hi : lo;
     off[i][1] = swap ? lo : hi;
   }
-  uint8_t *R = smem + kOffR;
   uint8_t *Qs = smem + kOffQ;
   const int *lists = reinterpret_cast<const int *>(smem + kOffList);
   uint32_t g = 0;  // chunks produced by this CTA
@@ -360,7 +370,12 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms) {
         *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
       }
     }
+    // ---- row list and counts of this query (built one query ahead by the
+    // first softmax warp)
+    const uint32_t ms_slot = qi & 1;
+    const bool meta_ok = wait_bar(&ms->meta_full[ms_slot], (qi >> 1) & 1, ms);
     asm volatile("cp.async.wait_all;" ::: "memory");
+    if (!meta_ok) break;
     for (int it = ptid; it < P.n_heads * (kDim / 8); it += kProducerThreads) {
       const int h = it / (kDim / 8), d = (it % (kDim / 8)) * 8;
       uint4 *p4 = reinterpret_cast<uint4 *>(Qs + sw128_offset(h, d, kQBlock));
@@ -378,11 +393,6 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms) {
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&ms->q_full);
-    // ---- row list (first producer warp), shared with the other producers
-    // ---- row list and counts of this query (built one query ahead by the
-    // first softmax warp)
-    const uint32_t ms_slot = qi & 1;
-    if (!wait_bar(&ms->meta_full[ms_slot], (qi >> 1) & 1, ms)) break;
     const int *list = lists + ms_slot * kMaxSel;
     Src S;
     S.nsel = ms->meta[ms_slot][0];
@@ -396,32 +406,31 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms) {
     S.dummy_b = P.swa_fp8 + seg * 16;
     S.dummy_s = P.swa_scale + seg / 2;
     const int nch = n_chunks_of(S.nrows);
-    // ---- chunks: 4 steps of 128 channels each; the loads of the next two
-    // steps are in flight while a step waits for its buffer and is stored
-    const int nsteps = nch * 4;
-    Item b0[kItemsPerThread], b1[kItemsPerThread], b2[kItemsPerThread];
-    load_step(list, S, row0, 0, 0, b0);
-    if (nsteps > 1) load_step(list, S, row0, 0, 1, b1);
+    // ---- chunks: 2 steps of 32 rows each; the loads of the next step are
+    // in flight while a step waits for its buffer and is stored
+    const int nsteps = nch * 2;
+    Item b0[kItemsPerThread], b1[kItemsPerThread];
+    load_step(list, S, row0, 0, b0);
     bool ok = true;
-    // one step: prefetch step st+2 into `pre`, then store step st from `use`
+    // one step: prefetch step st+1 into `pre`, then store step st from `use`
     auto step = [&](int st, Item(&use)[kItemsPerThread], Item(&pre)[kItemsPerThread]) -> bool {
-      const int c = st >> 2, pair = st & 3;
-      if (st + 2 < nsteps) load_step(list, S, row0, (st + 2) >> 2, (st + 2) & 3, pre);
-      if (!wait_bar(&ms->r_empty[pair], ((g + c) & 1) ^ 1, ms)) return false;
-      const int64_t valid_rows = S.nrows - (int64_t)c * kRowsPerChunk;
-      if (valid_rows >= kRowsPerChunk)
-        store_step<false>(R, pair, swap, row0, off, valid_rows, use);
+      const uint32_t gc = g + (uint32_t)(st >> 1), buf = gc & 1;
+      if (st + 1 < nsteps) load_step(list, S, row0, st + 1, pre);
+      if (!wait_bar(&ms->r_empty[buf], ((gc >> 1) & 1) ^ 1, ms)) return false;
+      uint8_t *R = smem + kOffR + buf * kRBuf;
+      const int64_t valid_rows = S.nrows - (int64_t)st * kStepRows;
+      if (valid_rows >= kStepRows)
+        store_step<false>(R, st & 1, swap, row0, off, valid_rows, use);
       else
-        store_step<true>(R, pair, swap, row0, off, valid_rows, use);
+        store_step<true>(R, st & 1, swap, row0, off, valid_rows, use);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ms->r_full[pair]);
+      if (lane == 0) mbar_arrive(&ms->r_full[buf]);
       return true;
     };
-    for (int st = 0; st < nsteps && ok; st += 3) {
-      ok = step(st, b0, b2);
+    for (int st = 0; st < nsteps && ok; st += 2) {
+      ok = step(st, b0, b1);
       if (ok && st + 1 < nsteps) ok = step(st + 1, b1, b0);
-      if (ok && st + 2 < nsteps) ok = step(st + 2, b2, b1);
     }
     g += nch;
     if (!ok) break;
@@ -429,84 +438,111 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms) {
 }
 
 // ---------------------------------------------------------------------------
-// MMA issuer: the whole warp walks the queries (row counts need the warp),
-// lane 0 waits on the barriers and issues every MMA and commit.
+// MMA issuer: lane 0 of the warp.  S^T of chunk g is issued before O^T of
+// chunk g-1 (S^T runs one chunk ahead); at a query boundary the pending O^T is
+// issued first so the epilogue of the finished query is not held back.
 // ---------------------------------------------------------------------------
-__device__ void mma_role(const Params &P, uint8_t *smem, Misc *ms) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t tmem = ms->tmem_base;
+// Operand descriptors: bases (low, high words); every MMA's descriptor is
+// one of these plus a compile-time offset in the low word.
+struct Descs {
+  uint32_t rk_lo, rk_hi, q_lo, q_hi, rm_lo, rm_hi, p_lo, p_hi;
+};
+
+__device__ __forceinline__ Descs make_descs(uint8_t *smem) {
   const uint32_t r0 = smem_u32(smem + kOffR), q0 = smem_u32(smem + kOffQ),
                  p0 = smem_u32(smem + kOffP);
-  const uint32_t id_s = make_idesc_f16(128, kHeadsPad, false, false);
-  const uint32_t id_o = make_idesc_f16(128, kHeadsPad, true, true);
-  // base descriptors; every MMA's operand descriptor is one of these plus a
-  // compile-time offset
   const uint64_t d_rk = make_desc_sw128(r0, 16, 1024);        // R, K-major (S)
   const uint64_t d_q = make_desc_sw128(q0, 16, 1024);         // Q, K-major (S)
   const uint64_t d_rm = make_desc_sw128(r0, kRBlock, 1024);   // R^T, MN-major (O)
   const uint64_t d_p = make_desc_sw128(p0, kRBlock, 1024);    // P^T, MN-major (O)
-  const uint32_t rk_lo = (uint32_t)d_rk, rk_hi = (uint32_t)(d_rk >> 32);
-  const uint32_t q_lo = (uint32_t)d_q, q_hi = (uint32_t)(d_q >> 32);
-  const uint32_t rm_lo = (uint32_t)d_rm, rm_hi = (uint32_t)(d_rm >> 32);
-  const uint32_t p_lo = (uint32_t)d_p, p_hi = (uint32_t)(d_p >> 32);
-  uint32_t g = 0, qi = 0;
-  int ok = 1;
-  for (int q = blockIdx.x; q < P.b.num_q && lane == 0; q += gridDim.x, ++qi) {
-    {
+  return Descs{(uint32_t)d_rk, (uint32_t)(d_rk >> 32), (uint32_t)d_q, (uint32_t)(d_q >> 32),
+               (uint32_t)d_rm, (uint32_t)(d_rm >> 32), (uint32_t)d_p, (uint32_t)(d_p >> 32)};
+}
+
+// bounded wait for every MMA this thread issued (TMEM is never freed under a
+// running MMA)
+__device__ __forceinline__ void drain(uint64_t *bar) {
+  mma_commit(bar);
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, 0) && globaltimer() - t0 < kWaitNs) {
+  }
+}
+
+// S^T issuer (lane 0 of warp kMmaWarp): S^T(g) = R(g) . Q^T into S buffer g&1
+// as soon as chunk g is produced and the buffer is free.
+__device__ void s_issuer_role(const Params &P, uint8_t *smem, Misc *ms) {
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) {
+    const uint32_t tmem = ms->tmem_base;
+    const uint32_t id_s = make_idesc_f16(kChunk, kHeadsPad, false, false);
+    const Descs D = make_descs(smem);
+    bool ok = true;
+    uint32_t g = 0, qi = 0;
+    for (int q = blockIdx.x; q < P.b.num_q && ok; q += gridDim.x, ++qi) {
       const uint32_t slot = qi & 1;
       if (!(ok = wait_bar(&ms->meta_full[slot], (qi >> 1) & 1, ms))) break;
       const int nch = n_chunks_of(ms->meta[slot][0] + ms->meta[slot][1]);
       for (int c = 0; c < nch && ok; ++c, ++g) {
-        const uint32_t sb = g & 1;
-        const uint32_t s_tmem = tmem + kColS + sb * 64;
-        // ---- S^T(c) = R . Q^T into S buffer sb
-        ok = wait_bar(&ms->s_empty[sb], ((g >> 1) & 1) ^ 1, ms);
+        const uint32_t sb = g & 1, ph = (g >> 1) & 1;
+        ok = wait_bar(&ms->s_empty[sb], ph ^ 1, ms);
         if (ok && c == 0) ok = wait_bar(&ms->q_full, qi & 1, ms);
-        for (int pair = 0; pair < 4 && ok; ++pair) {
-          ok = wait_bar(&ms->r_full[pair], g & 1, ms);
-          if (!ok) break;
-          fence_after_sync();
-          const uint32_t a_p = rk_lo + ((pair * 2 * kRBlock) >> 4);
-          const uint32_t b_p = q_lo + ((pair * 2 * kQBlock) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t oa = ((kk >> 2) * kRBlock + (kk & 3) * 32) >> 4;
-            const uint32_t ob = ((kk >> 2) * kQBlock + (kk & 3) * 32) >> 4;
-            mma_f16_split(s_tmem, a_p + oa, rk_hi, b_p + ob, q_hi, id_s,
-                          (pair > 0 || kk > 0) ? 1u : 0u);
-          }
-        }
+        if (ok) ok = wait_bar(&ms->r_full[sb], ph, ms);
         if (!ok) break;
+        fence_after_sync();
+        const uint32_t ra = D.rk_lo + ((sb * kRBuf) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 32; ++kk) {
+          const int blk = kk >> 2;
+          mma_f16_split(tmem + kColS + sb * 64, ra + ((blk * kRBlock + (kk & 3) * 32) >> 4),
+                        D.rk_hi, D.q_lo + ((blk * kQBlock + (kk & 3) * 32) >> 4), D.q_hi, id_s,
+                        kk > 0 ? 1u : 0u);
+        }
         mma_commit(&ms->s_full[sb]);
         if (c == nch - 1) mma_commit(&ms->q_empty);
-        // ---- O^T += R^T . P^T, 4 tiles of 128 channels
-        ok = wait_bar(&ms->p_full, g & 1, ms);
+      }
+    }
+    drain(&ms->done);
+  }
+  __syncwarp();
+}
+
+// O^T issuer (lane 0 of warp kOWarp): O^T += R(g)^T . P(g)^T as soon as P(g) is
+// written.  S^T(g) has completed by then (the softmax read it), so this
+// issuer's commit releases R(g) for both products.
+__device__ void o_issuer_role(const Params &P, uint8_t *smem, Misc *ms) {
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) {
+    const uint32_t tmem = ms->tmem_base;
+    const uint32_t id_o = make_idesc_f16(128, kHeadsPad, true, true);
+    const Descs D = make_descs(smem);
+    bool ok = true;
+    uint32_t g = 0, qi = 0;
+    for (int q = blockIdx.x; q < P.b.num_q && ok; q += gridDim.x, ++qi) {
+      const uint32_t slot = qi & 1;
+      if (!(ok = wait_bar(&ms->meta_full[slot], (qi >> 1) & 1, ms))) break;
+      const int nch = n_chunks_of(ms->meta[slot][0] + ms->meta[slot][1]);
+      for (int c = 0; c < nch && ok; ++c, ++g) {
+        const uint32_t buf = g & 1, ph = (g >> 1) & 1;
+        ok = wait_bar(&ms->p_full[buf], ph, ms);
         if (ok && c == 0) ok = wait_bar(&ms->o_empty, (qi & 1) ^ 1, ms);
         if (!ok) break;
         fence_after_sync();
+        const uint32_t ra = D.rm_lo + ((buf * kRBuf) >> 4), pa = D.p_lo + ((buf * kPBuf) >> 4);
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            mma_f16_split(tmem + kColO + t * 64, rm_lo + ((t * 2 * kRBlock + ks * 2048) >> 4),
-                          rm_hi, p_lo + ((ks * 2048) >> 4), p_hi, id_o,
+          for (int ks = 0; ks < kChunk / 16; ++ks) {
+            mma_f16_split(tmem + kColO + t * 64, ra + ((t * 2 * kRBlock + ks * 2048) >> 4),
+                          D.rm_hi, pa + ((ks * 2048) >> 4), D.p_hi, id_o,
                           (c > 0 || ks > 0) ? 1u : 0u);
           }
-          mma_commit(&ms->r_empty[t]);
         }
-        mma_commit(&ms->p_empty);
+        mma_commit(&ms->r_empty[buf]);
+        mma_commit(&ms->p_empty[buf]);
         if (c == nch - 1) mma_commit(&ms->o_full);
       }
     }
-    if (!ok) break;
-  }
-  // drain: every MMA issued so far has completed once `done` flips (bounded
-  // by time only, so that TMEM is never freed under a running MMA)
-  if (lane == 0) {
-    mma_commit(&ms->done);
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(&ms->done, 0) && globaltimer() - t0 < kWaitNs) {
-    }
+    drain(&ms->done_o);
   }
   __syncwarp();
 }
@@ -521,7 +557,6 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
   const int stid = threadIdx.x;     // 0..255
   const uint32_t tmem = ms->tmem_base;
   const uint32_t lane_addr = (uint32_t)(32 * sp) << 16;
-  uint8_t *Pbuf = smem + kOffP;
   const float NEG_INF = -INFINITY;
   float lsum[32];
   uint32_t g = 0, qi = 0, gp = 0;
@@ -558,8 +593,8 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) lsum[j] = 0.f;
     for (int c = 0; c < nch; ++c, ++g) {
-      const uint32_t sb = g & 1;
-      ok = wait_bar(&ms->s_full[sb], (g >> 1) & 1, ms);
+      const uint32_t sb = g & 1, ph = (g >> 1) & 1;
+      ok = wait_bar(&ms->s_full[sb], ph, ms);
       if (!ok) break;
       fence_after_sync();
       uint32_t v[32];
@@ -568,8 +603,9 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ms->s_empty[sb]);
-      const int64_t row = (int64_t)c * kRowsPerChunk + 32 * sp + lane;
-      const bool valid = row < nrows;
+      // M = 64 layout: lanes 0-15 of this sub-partition hold rows 16*sp + lane
+      const int crow = 16 * sp + lane;
+      const bool valid = lane < 16 && (int64_t)c * kChunk + crow < nrows;
       float x[32];
       bool exceed = false;
 #pragma unroll
@@ -586,7 +622,7 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
 #pragma unroll
       for (int w = 0; w < kSoftmaxWarps; ++w) slow |= ms->votes[vb][w] != 0;
       if (slow) {
-        // per-head maximum over the warp's 32 rows (butterfly per head), then
+        // per-head maximum over the warp's rows (butterfly per head), then
         // across the 4 warps of this head half
         float mine = NEG_INF;
 #pragma unroll
@@ -609,27 +645,30 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
         if (!(ok = group_sync(&ms->sm_grp, gp, ms))) break;
 #pragma unroll
         for (int j = 0; j < 32; ++j) lsum[j] *= ms->alpha[32 * hh + j];
-      }
-      // P(c) may be written once O^T(c-1) has consumed P(c-1); that also
-      // means every earlier O^T MMA has completed (needed for a rescale)
-      ok = wait_bar(&ms->p_empty, (g & 1) ^ 1, ms);
-      if (!ok) break;
-      fence_after_sync();
-      if (slow && c > 0) {
+        if (c > 0) {
+          // every earlier O^T MMA of this query must be complete: the latest
+          // one issued is O^T(g-1)
+          const uint32_t pb = (g - 1) & 1;
+          if (!(ok = wait_bar(&ms->p_empty[pb], ((g - 1) >> 1) & 1, ms))) break;
+          fence_after_sync();
 #pragma unroll 1
-        for (int t = 0; t < 8; ++t) {   // 4 tiles x 2 halves of this warp's 32 heads
-          uint32_t o[32];
-          const int hb = 32 * hh + 16 * (t & 1);
-          const uint32_t a = tmem + lane_addr + kColO + (t >> 1) * 64 + 16 * (t & 1) + 32 * hh;
-          tmem_ld32x32b_x16(a, o);
-          tmem_wait_ld();
+          for (int t = 0; t < 8; ++t) {   // 4 tiles x 2 halves of this warp's 32 heads
+            uint32_t o[32];
+            const int hb = 32 * hh + 16 * (t & 1);
+            const uint32_t a = tmem + lane_addr + kColO + (t >> 1) * 64 + 16 * (t & 1) + 32 * hh;
+            tmem_ld32x32b_x16(a, o);
+            tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            o[j] = __float_as_uint(__uint_as_float(o[j]) * ms->alpha[hb + j]);
-          tmem_st32x32b_x16(a, o);
+            for (int j = 0; j < 16; ++j)
+              o[j] = __float_as_uint(__uint_as_float(o[j]) * ms->alpha[hb + j]);
+            tmem_st32x32b_x16(a, o);
+          }
+          tmem_wait_st();
         }
-        tmem_wait_st();
       }
+      // P(g) goes to buffer g&1 once O^T(g-2) has consumed it
+      ok = wait_bar(&ms->p_empty[sb], ph ^ 1, ms);
+      if (!ok) break;
       uint32_t pk[16];
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
@@ -641,15 +680,17 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
         __half2 h2 = __floats2half2_rn(p0, p1);
         pk[j / 2] = *reinterpret_cast<uint32_t *>(&h2);
       }
-      const int prow = 32 * sp + lane;
+      if (lane < 16) {
+        uint8_t *Pb = smem + kOffP + sb * kPBuf;
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        *reinterpret_cast<uint4 *>(Pbuf + sw128_offset(prow, 32 * hh + 8 * i, 0)) =
-            make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<uint4 *>(Pb + sw128_offset(crow, 32 * hh + 8 * i, 0)) =
+              make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      }
       fence_proxy_async_smem();
       fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ms->p_full);
+      if (lane == 0) mbar_arrive(&ms->p_full[sb]);
     }
     if (!ok) break;
     // ---- epilogue: row sums, normalisation, bf16 output, lse
@@ -708,21 +749,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(Params P) {
   if (threadIdx.x == 0) {
     mbar_init(&ms->q_full, kProducerWarps);
     mbar_init(&ms->q_empty, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&ms->s_full[i], 1);
-      mbar_init(&ms->s_empty[i], kSoftmaxWarps);
-    }
-    mbar_init(&ms->p_full, kSoftmaxWarps);
-    mbar_init(&ms->p_empty, 1);
     mbar_init(&ms->o_full, 1);
     mbar_init(&ms->o_empty, kSoftmaxWarps);
     mbar_init(&ms->done, 1);
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(&ms->r_full[i], kProducerWarps);
-      mbar_init(&ms->r_empty[i], 1);
-    }
+    mbar_init(&ms->done_o, 1);
     mbar_init(&ms->sm_grp, kSoftmaxWarps);
-    for (int i = 0; i < 2; ++i) mbar_init(&ms->meta_full[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ms->r_full[i], 2 * kProducerWarps);   // two steps per chunk
+      mbar_init(&ms->r_empty[i], 1);
+      mbar_init(&ms->s_full[i], 1);
+      mbar_init(&ms->s_empty[i], kSoftmaxWarps);
+      mbar_init(&ms->p_full[i], kSoftmaxWarps);
+      mbar_init(&ms->p_empty[i], 1);
+      mbar_init(&ms->meta_full[i], 1);
+    }
     ms->abort = 0;
     mbar_fence_init();
   }
@@ -736,7 +776,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(Params P) {
   if (warp < kSoftmaxWarps) {
     softmax_role(P, smem, ms);
   } else if (warp == kMmaWarp) {
-    mma_role(P, smem, ms);
+    s_issuer_role(P, smem, ms);
+  } else if (warp == kOWarp) {
+    o_issuer_role(P, smem, ms);
   } else {
     producer_role(P, smem, ms);
   }
