@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-fp4kv", action="store_true",
+                    help="skip the FP4 main-KV attention measurement")
     ap.add_argument("--no-cpu", action="store_true")
     return ap.parse_args()
 
@@ -127,10 +129,10 @@ def measured_peaks():
     return 6800.0, 1700.0, "fallback"
 
 
-def attn_algorithmic_bytes(w, runner, layer, win_lo):
+def attn_algorithmic_bytes(w, runner, layer, win_lo, sel_row_bytes=None):
     """Bytes the method itself reads and writes in one attention launch: per
-    query the selected rows plus its window rows (576 B each), Q and O (bf16),
-    the index row (int32) and the lse (fp32)."""
+    query the selected rows (576 B each, or sel_row_bytes) plus its window rows
+    (576 B each), Q and O (bf16), the index row (int32) and the lse (fp32)."""
     import torch
     nq = runner.nq
     pos = runner.batches[layer]["q_pos"].to(torch.int64)
@@ -144,7 +146,8 @@ def attn_algorithmic_bytes(w, runner, layer, win_lo):
     else:
         n_sel = int(runner.count[layer].sum())
     per_q = w.n_heads * 512 * 2 * 2 + w.topk * 4 + w.n_heads * 4
-    return (n_sel + n_win) * ROW_BYTES + nq * per_q
+    sel = ROW_BYTES if sel_row_bytes is None else sel_row_bytes
+    return n_sel * sel + n_win * ROW_BYTES + nq * per_q
 
 
 def bench_ours(args, rank, world, local_rank):
@@ -221,12 +224,49 @@ def bench_ours(args, rank, world, local_rank):
                 "avg_launch_ms": round(attn_avg_ms, 4),
                 "share_of_step": round(sum(attn_ms) / sum(step_ms), 3)}
 
+    fp4 = None if args.no_fp4kv else bench_fp4kv(args, w, run, stream, flush, hbm)
+
     e2e = None
     if not args.no_e2e:
         e2e = bench_e2e(args, w, run, dev, rank, world)
 
     return dict(value=value, ms=ms, wall=wall, clocks=clk, roofline=roofline, e2e=e2e,
-                launches=launches_per_step * args.steps, rows=rows, w=w)
+                launches=launches_per_step * args.steps, rows=rows, w=w, fp4kv=fp4)
+
+
+def bench_fp4kv(args, w, run, stream, flush, hbm):
+    """The FP4 main-KV layout (E2M1 + E4M3 scale per 16 channels, 288 B per
+    entry) on the same step's L22 attention: the Reuse layer's launch with the
+    Reindex indices and the tail window, selected rows read from an FP4 copy of
+    the same pool.  Timed per launch with events, L2 flushed between launches."""
+    import torch
+    from sparse_attention_prefill_gb300 import synth
+    from sparse_attention_prefill_gb300 import sparse_swa_attn_fp4kv
+    synth.with_fp4kv(w, args.seed)
+    L = w.layers["L22"]
+    q = run._lt("L22", "q")
+    idx = run.idx["L21"]
+    args_ = (run.batches["L22"], q, w.pool.kv_fp4, w.pool.kv_sf, idx, L.swa_fp8, L.swa_scale,
+             run.tail_win_lo, w.window, w.sm_scale)
+    out, lse = run.out["L22"], run.lse["L22"]
+    for _ in range(3):
+        sparse_swa_attn_fp4kv(*args_, out=out, lse=lse, d_err=run.d_err)
+    ts = []
+    for _ in range(max(5, min(args.steps, 20))):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        sparse_swa_attn_fp4kv(*args_, out=out, lse=lse, d_err=run.d_err)
+        e1.record(stream)
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    assert int(run.d_err.item()) == 0
+    ms = sum(a.elapsed_time(b) for a, b in ts) / len(ts)
+    byts = attn_algorithmic_bytes(w, run, "L22", run.tail_win_lo, sel_row_bytes=288)
+    return {"kernel": "csa2_sparse_swa_attn_fp4kv", "layer": "L22 (Reuse, tail window)",
+            "avg_launch_ms": round(ms, 4), "algorithmic_bytes_per_launch": int(byts),
+            "achieved_gbs": round(byts / (ms * 1e-3) / 1e9, 1), "peak_gbs": hbm,
+            "frac": round(byts / (ms * 1e-3) / 1e9 / hbm, 4)}
 
 
 def run_kernel_id():
@@ -453,7 +493,7 @@ def main():
                 "config": config_block(r["w"], {"parallelism": "replicas" if world > 1 else "1gpu"}),
                 "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r["e2e"],
                 "clocks": r["clocks"], "gpu_launches": r["launches"],
-                "wall_s_timed_region": round(r["wall"], 4)}
+                "wall_s_timed_region": round(r["wall"], 4), "fp4_kv_attention": r["fp4kv"]}
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

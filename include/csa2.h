@@ -234,6 +234,28 @@ CSA2_API int csa2_sparse_swa_attn(const csa2_batch *b, int32_t n_heads, int32_t 
                          const float *sink, void *out_bf16, float *lse,
                          int32_t *d_err, csa2_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * a10 with the FP4 main-KV layout  [CSA2] mixed-precision card ("Main KV:
+ * E2M1 数据；每 16 通道一个 E4M3 scale；省略 NVFP4 的二级全局 scale";
+ * 512 x (0.5 + 1/16) = 288 B per entry; SWA stays FP8).
+ *
+ * The same attention as csa2_sparse_swa_attn, with the selected rows read from
+ * an FP4 pool:
+ *   kv_fp4 [Nkv, dim/2]  E2M1 codes, element 2i in the low nibble of byte i
+ *   kv_sf  [Nkv, dim/16] E4M3 (OCP "FN") scale codes, one per 16 channels
+ *   row element d = e2m1(code d) * e4m3(kv_sf[d/16])
+ * Window rows are FP8 block-32 as in csa2_sparse_swa_attn.  Every other
+ * argument, layout, error and limit is that function's.  kv_fp4 must be
+ * 8-byte aligned.
+ * ------------------------------------------------------------------------- */
+CSA2_API int csa2_sparse_swa_attn_fp4kv(const csa2_batch *b, int32_t n_heads, int32_t dim,
+                         const void *q_bf16, const uint8_t *kv_fp4,
+                         const uint8_t *kv_sf, const int32_t *idx, int32_t k,
+                         const uint8_t *swa_fp8, const float *swa_scale,
+                         const int64_t *win_lo, int32_t window, float sm_scale,
+                         const float *sink, void *out_bf16, float *lse,
+                         int32_t *d_err, csa2_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -37,8 +37,10 @@ def lib():
         _lib.oracle_n_visible.restype = C.c_int64
         _lib.oracle_n_visible.argtypes = [C.c_int64, C.c_int]
         for name in ("oracle_tail_layout", "oracle_index_score", "oracle_topk",
-                     "oracle_topk_candidates", "oracle_sparse_swa_attn"):
+                     "oracle_topk_candidates", "oracle_sparse_swa_attn",
+                     "oracle_sparse_swa_attn_fp4kv"):
             getattr(_lib, name).restype = C.c_int
+        _lib.oracle_decode_fp4kv_row.restype = None
     return _lib
 
 
@@ -179,3 +181,37 @@ def sparse_swa_attn(b, q_bf16, kv_fp8, kv_scale, idx, swa_fp8, swa_scale, win_lo
                                        _p(wl), C.c_int(window), C.c_double(sm_scale), _p(sk),
                                        _p(out), _p(lse))
     return out, lse, err
+
+
+def sparse_swa_attn_fp4kv(b, q_bf16, kv_fp4, kv_sf, idx, swa_fp8, swa_scale, win_lo=None,
+                          window=128, sm_scale=None, sink=None, want_lse=True):
+    """As ``sparse_swa_attn`` with the selected rows taken from the FP4 main-KV
+    pool: ``kv_fp4`` uint8 [Nkv, D/2] E2M1 pairs, ``kv_sf`` uint8 [Nkv, D/16]
+    E4M3 scales (one per 16 channels)."""
+    st, keep = _batch(b)
+    q = _c(q_bf16, np.uint16)
+    nq, n_heads, dim = q.shape
+    if sm_scale is None:
+        sm_scale = 1.0 / np.sqrt(dim)
+    kvf, kvs = _c(kv_fp4, np.uint8), _c(kv_sf, np.uint8)
+    sf, ss = _c(swa_fp8, np.uint8), _c(swa_scale, np.float32)
+    ix = _c(idx, np.int32)
+    k = 0 if ix is None else ix.shape[1]
+    wl = _c(win_lo, np.int64)
+    sk = _c(sink, np.float32)
+    out = np.zeros((nq, n_heads, dim), np.uint16)
+    lse = np.zeros((nq, n_heads), np.float32) if want_lse else None
+    err = lib().oracle_sparse_swa_attn_fp4kv(C.byref(st), C.c_int(n_heads), C.c_int(dim), _p(q),
+                                             _p(kvf), _p(kvs), _p(ix), C.c_int(k), _p(sf),
+                                             _p(ss), _p(wl), C.c_int(window),
+                                             C.c_double(sm_scale), _p(sk), _p(out), _p(lse))
+    return out, lse, err
+
+
+def decode_fp4kv_row(codes, sf):
+    """One FP4 main-KV row decoded to float64 (codes uint8 [D/2], sf uint8 [D/16])."""
+    c, f = _c(codes, np.uint8), _c(sf, np.uint8)
+    dim = c.shape[-1] * 2
+    out = np.zeros(dim, np.float64)
+    lib().oracle_decode_fp4kv_row(_p(c), _p(f), C.c_int(dim), _p(out))
+    return out

@@ -16,7 +16,9 @@
  *                    S-T, visible window [max(s, i-127), i].
  *   index formats    "DeepSeek V4.1 Flash 建模" (pages.haorui.li), mixed-precision
  *                    card: indexer Q/K are MXFP4 with 32-element groups; main KV
- *                    here is E4M3 with one scale per 32 channels (block-32).
+ *                    is E4M3 with one scale per 32 channels (block-32), or, in
+ *                    the card's own layout, E2M1 with one E4M3 scale per 16
+ *                    channels (288 B per entry); SWA rows stay FP8.
  *   index score      same page, CSA2 and Hierarchical Sparse Indexer cards; SGLang/
  *                    Miles day-0 article (theainews.cc) sec. 2 and sec. 5 ("FP4
  *                    索引与 TP 布局": MQA-shaped indexer, heads replicated, a
@@ -96,6 +98,22 @@ static double mxfp4_elem(const uint8_t *codes, const float *scales, int d) {
 /* Element d of an FP8 block-32 row. */
 static double fp8_elem(const uint8_t *codes, const float *scales, int d) {
   return oracle_e4m3_value(codes[d]) * (double)scales[d / 32];
+}
+
+/* Element d of an FP4 main-KV row ("DeepSeek V4.1 Flash 建模", mixed-precision
+ * card, Main KV row: E2M1 data, one E4M3 scale per 16 channels, no second-level
+ * global scale; 512 x (0.5 + 1/16) = 288 B per entry).  Byte d/2 holds element
+ * 2i in its low nibble and element 2i+1 in its high nibble (as the index rows). */
+static double fp4kv_elem(const uint8_t *codes, const uint8_t *sf, int d) {
+  int byte = codes[d / 2];
+  int nib = (d & 1) ? (byte >> 4) : (byte & 15);
+  return oracle_e2m1_value(nib) * oracle_e4m3_value(sf[d / 16]);
+}
+
+/* One FP4 main-KV row of `dim` elements decoded to double (used by the pins). */
+void oracle_decode_fp4kv_row(const uint8_t *codes, const uint8_t *sf, int dim,
+                             double *out) {
+  for (int d = 0; d < dim; ++d) out[d] = fp4kv_elem(codes, sf, d);
 }
 
 /* bf16 -> double (exact) and double -> bf16 with round-to-nearest-even. */
@@ -409,12 +427,15 @@ int oracle_topk_candidates(const oracle_batch *b, const float *scores,
  * window positions without a stored SWA row are skipped (error bit 2).  A
  * query with no rows and no sink gets O = 0 and lse = -inf.  O is rounded to
  * bf16 (RNE), lse stored as float. */
-int oracle_sparse_swa_attn(const oracle_batch *b, int n_heads, int dim,
-                           const uint16_t *q_bf16, const uint8_t *kv_fp8,
-                           const float *kv_scale, const int32_t *idx, int k,
-                           const uint8_t *swa_fp8, const float *swa_scale,
-                           const int64_t *win_lo, int window, double sm_scale,
-                           const float *sink, uint16_t *out_bf16, float *lse) {
+/* Selected rows come from the main KV pool in one of two formats: FP8 block-32
+ * (kv_codes [Nkv, dim] E4M3 + kv_scales fp32 [Nkv, dim/32]) or FP4
+ * (kv_codes [Nkv, dim/2] E2M1 + kv_sf E4M3 [Nkv, dim/16]).  Window rows are
+ * always FP8 block-32 (mixed-precision card: SWA stays FP8). */
+static int attn_core(const oracle_batch *b, int n_heads, int dim, const uint16_t *q_bf16,
+                     int kv_fp4, const uint8_t *kv_codes, const float *kv_scale,
+                     const uint8_t *kv_sf, const int32_t *idx, int k, const uint8_t *swa_fp8,
+                     const float *swa_scale, const int64_t *win_lo, int window,
+                     double sm_scale, const float *sink, uint16_t *out_bf16, float *lse) {
   int err = 0;
   const int nsc = dim / 32;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
@@ -436,7 +457,8 @@ int oracle_sparse_swa_attn(const oracle_batch *b, int n_heads, int dim,
       int64_t row = b->kv_start[r] + j;
       for (int d = 0; d < dim; ++d)
         rows[(size_t)nrows * dim + d] =
-            fp8_elem(kv_fp8 + row * dim, kv_scale + row * nsc, d);
+            kv_fp4 ? fp4kv_elem(kv_codes + row * (dim / 2), kv_sf + row * (dim / 16), d)
+                   : fp8_elem(kv_codes + row * dim, kv_scale + row * nsc, d);
       ++nrows;
     }
     /* the query's own sliding window */
@@ -491,4 +513,25 @@ int oracle_sparse_swa_attn(const oracle_batch *b, int n_heads, int dim,
     free(o);
   }
   return err;
+}
+
+int oracle_sparse_swa_attn(const oracle_batch *b, int n_heads, int dim,
+                           const uint16_t *q_bf16, const uint8_t *kv_fp8,
+                           const float *kv_scale, const int32_t *idx, int k,
+                           const uint8_t *swa_fp8, const float *swa_scale,
+                           const int64_t *win_lo, int window, double sm_scale,
+                           const float *sink, uint16_t *out_bf16, float *lse) {
+  return attn_core(b, n_heads, dim, q_bf16, 0, kv_fp8, kv_scale, NULL, idx, k, swa_fp8,
+                   swa_scale, win_lo, window, sm_scale, sink, out_bf16, lse);
+}
+
+/* The same attention with the selected rows read from the FP4 main-KV pool. */
+int oracle_sparse_swa_attn_fp4kv(const oracle_batch *b, int n_heads, int dim,
+                                 const uint16_t *q_bf16, const uint8_t *kv_fp4,
+                                 const uint8_t *kv_sf, const int32_t *idx, int k,
+                                 const uint8_t *swa_fp8, const float *swa_scale,
+                                 const int64_t *win_lo, int window, double sm_scale,
+                                 const float *sink, uint16_t *out_bf16, float *lse) {
+  return attn_core(b, n_heads, dim, q_bf16, 1, kv_fp4, NULL, kv_sf, idx, k, swa_fp8,
+                   swa_scale, win_lo, window, sm_scale, sink, out_bf16, lse);
 }

@@ -25,7 +25,7 @@ DERR_RANGE_IDX, DERR_RANGE_WINDOW, DERR_RANGE_CTX = 1, 2, 4
 DERR_SCALE, DERR_LD, DERR_CAPACITY, DERR_BAD_EXTEND = 8, 16, 32, 64
 
 EXPORTED = ("csa2_status_string", "csa2_tail_layout", "csa2_index_score", "csa2_topk",
-            "csa2_topk_candidates", "csa2_sparse_swa_attn")
+            "csa2_topk_candidates", "csa2_sparse_swa_attn", "csa2_sparse_swa_attn_fp4kv")
 
 
 class Csa2Error(RuntimeError):
@@ -63,6 +63,7 @@ def load(path: Optional[str] = None):
     lib.csa2_topk_candidates.argtypes = [vp, vp, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp]
     lib.csa2_sparse_swa_attn.argtypes = [vp, i32, i32, vp, vp, vp, vp, i32, vp, vp, vp, i32, f32,
                                          vp, vp, vp, vp, vp]
+    lib.csa2_sparse_swa_attn_fp4kv.argtypes = lib.csa2_sparse_swa_attn.argtypes
     for name in EXPORTED[1:]:
         getattr(lib, name).restype = C.c_int
     _lib = lib
@@ -153,6 +154,18 @@ def csa2_sparse_swa_attn(batch, n_heads, dim, q_bf16, kv_fp8, kv_scale, idx, k, 
                                        _ptr(d_err), _stream(stream))
 
 
+def csa2_sparse_swa_attn_fp4kv(batch, n_heads, dim, q_bf16, kv_fp4, kv_sf, idx, k, swa_fp8,
+                               swa_scale, win_lo, window, sm_scale, sink, out_bf16, lse, d_err,
+                               stream=None) -> int:
+    st, keep = make_batch(batch)
+    return load().csa2_sparse_swa_attn_fp4kv(C.byref(st), int(n_heads), int(dim), _ptr(q_bf16),
+                                             _ptr(kv_fp4), _ptr(kv_sf), _ptr(idx), int(k),
+                                             _ptr(swa_fp8), _ptr(swa_scale), _ptr(win_lo),
+                                             int(window), float(sm_scale), _ptr(sink),
+                                             _ptr(out_bf16), _ptr(lse), _ptr(d_err),
+                                             _stream(stream))
+
+
 # ---------------------------------------------------------------------------
 # allocating conveniences (torch allocates the outputs; the library computes)
 # ---------------------------------------------------------------------------
@@ -225,4 +238,23 @@ def sparse_swa_attn(batch, q, kv_fp8, kv_scale, idx, swa_fp8, swa_scale, win_lo=
     _check(csa2_sparse_swa_attn(batch, n_heads, dim, q, kv_fp8, kv_scale, idx, k, swa_fp8,
                                 swa_scale, win_lo, window, sm_scale, sink, out, lse, d_err,
                                 stream), "csa2_sparse_swa_attn")
+    return out, lse
+
+
+def sparse_swa_attn_fp4kv(batch, q, kv_fp4, kv_sf, idx, swa_fp8, swa_scale, win_lo=None,
+                          window=128, sm_scale=None, sink=None, out=None, lse=None,
+                          want_lse=True, d_err=None, stream=None):
+    """Attention with the selected rows read from the FP4 main-KV pool
+    (E2M1 codes [Nkv, 256] and E4M3 scales per 16 channels [Nkv, 32])."""
+    nq, n_heads, dim = q.shape
+    if sm_scale is None:
+        sm_scale = dim ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((nq, n_heads), dtype=torch.float32, device=q.device)
+    k = 0 if idx is None else int(idx.shape[1])
+    _check(csa2_sparse_swa_attn_fp4kv(batch, n_heads, dim, q, kv_fp4, kv_sf, idx, k, swa_fp8,
+                                      swa_scale, win_lo, window, sm_scale, sink, out, lse, d_err,
+                                      stream), "csa2_sparse_swa_attn_fp4kv")
     return out, lse

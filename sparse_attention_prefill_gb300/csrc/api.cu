@@ -76,7 +76,31 @@ extern "C" CSA2_API int csa2_sparse_swa_attn(const csa2_batch *b, int32_t n_head
   if (k > 2048 || window > 1024) return CSA2_ERR_UNSUPPORTED;
   const csa2::Batch v = csa2::to_device_view(b);
   return csa2::attn_tc(v, n_heads, reinterpret_cast<const __nv_bfloat16 *>(q_bf16), kv_fp8,
-                         kv_scale, idx, k, swa_fp8, swa_scale, win_lo, window, sm_scale, sink,
-                         reinterpret_cast<__nv_bfloat16 *>(out_bf16), lse, d_err,
+                         kv_scale, nullptr, idx, k, swa_fp8, swa_scale, win_lo, window, sm_scale,
+                         sink, reinterpret_cast<__nv_bfloat16 *>(out_bf16), lse, d_err,
                          csa2::as_stream(stream));
+}
+
+extern "C" CSA2_API int csa2_sparse_swa_attn_fp4kv(
+    const csa2_batch *b, int32_t n_heads, int32_t dim, const void *q_bf16, const uint8_t *kv_fp4,
+    const uint8_t *kv_sf, const int32_t *idx, int32_t k, const uint8_t *swa_fp8,
+    const float *swa_scale, const int64_t *win_lo, int32_t window, float sm_scale,
+    const float *sink, void *out_bf16, float *lse, int32_t *d_err, csa2_stream_t stream) {
+  if (!csa2::batch_ok(b, true) || window < 1) return CSA2_ERR_INVALID_ARG;
+  if (!idx) k = 0;
+  if (k < 0) return CSA2_ERR_INVALID_ARG;
+  if (b->num_q > 0 && (!q_bf16 || !swa_fp8 || !swa_scale || !out_bf16)) return CSA2_ERR_INVALID_ARG;
+  if (b->num_q > 0 && k > 0 && (!kv_fp4 || !kv_sf)) return CSA2_ERR_INVALID_ARG;
+  if (dim != 512) return CSA2_ERR_UNSUPPORTED;
+  if (n_heads != 16 && n_heads != 32 && n_heads != 64) return CSA2_ERR_UNSUPPORTED;
+  if (k > 2048 || window > 1024) return CSA2_ERR_UNSUPPORTED;
+  const csa2::Batch v = csa2::to_device_view(b);
+  // a null scale pointer selects the FP8 pool, so with no selected rows any
+  // readable byte stands in for it
+  const uint8_t *sf = kv_sf ? kv_sf : swa_fp8;
+  return csa2::attn_tc(v, n_heads, reinterpret_cast<const __nv_bfloat16 *>(q_bf16),
+                       kv_fp4 ? kv_fp4 : swa_fp8, nullptr, sf, idx, k, swa_fp8, swa_scale,
+                       win_lo, window, sm_scale, sink,
+                       reinterpret_cast<__nv_bfloat16 *>(out_bf16), lse, d_err,
+                       csa2::as_stream(stream));
 }

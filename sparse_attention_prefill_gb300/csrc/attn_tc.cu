@@ -192,8 +192,9 @@ struct Params {
   Batch b;
   int n_heads;
   const __nv_bfloat16 *q;
-  const uint8_t *kv_fp8;
+  const uint8_t *kv_fp8;     // FP8 rows, or E2M1 pairs when kv_sf is set
   const float *kv_scale;
+  const uint8_t *kv_sf;      // FP4 main KV: E4M3 scale per 16 channels
   const int32_t *idx;
   int k;
   const uint8_t *swa_fp8;
@@ -244,7 +245,8 @@ static_assert(kProducerThreads % 32 == 0, "segment fixed per thread");
 // Per-thread, per-query source bases (segment offset folded in).
 struct Src {
   const uint8_t *sel_b;   // row kv0 of the pool
-  const float *sel_s;
+  const float *sel_s;     // (FP8 main KV)
+  const uint8_t *sel_sf;  // (FP4 main KV)
   const uint8_t *win_b;   // first window row of the SWA buffer
   const float *win_s;
   const uint8_t *dummy_b; // a readable row for rows past the end (masked when stored)
@@ -252,6 +254,14 @@ struct Src {
   int64_t nsel, nrows;
 };
 
+// FP4 main-KV rows: 16 channels = 8 bytes of E2M1 pairs and one E4M3 scale
+// byte; the item holds them in codes.x/.y and codes.z.
+__device__ __forceinline__ void load_fp4(const Src &S, int64_t j, Item &it) {
+  const uint2 c = __ldg(reinterpret_cast<const uint2 *>(S.sel_b + j * (kDim / 2)));
+  it.codes = make_uint4(c.x, c.y, (uint32_t)__ldg(S.sel_sf + j * (kDim / 16)), 0u);
+}
+
+template <bool kFp4>
 __device__ __forceinline__ void load_step(const int *list, const Src &S, int row0, int step,
                                           Item (&it)[kItemsPerThread]) {
   const int64_t r0 = (int64_t)step * kStepRows;
@@ -260,8 +270,12 @@ __device__ __forceinline__ void load_step(const int *list, const Src &S, int row
     for (int i = 0; i < kItemsPerThread; ++i) {
       if (row0 + i * kRowStride < kStepRows) {
         const int64_t j = list[r0 + row0 + i * kRowStride];
-        it[i].codes = __ldg(reinterpret_cast<const uint4 *>(S.sel_b + j * kDim));
-        it[i].scale = __ldg(S.sel_s + j * (kDim / 32));
+        if (kFp4) {
+          load_fp4(S, j, it[i]);
+        } else {
+          it[i].codes = __ldg(reinterpret_cast<const uint4 *>(S.sel_b + j * kDim));
+          it[i].scale = __ldg(S.sel_s + j * (kDim / 32));
+        }
       }
     }
   } else if (r0 >= S.nsel && r0 + kStepRows <= S.nrows) {   // every row in the window
@@ -280,6 +294,10 @@ __device__ __forceinline__ void load_step(const int *list, const Src &S, int row
         const int64_t ri = r0 + row0 + i * kRowStride;
         const uint8_t *b;
         const float *sc;
+        if (kFp4 && ri < S.nsel) {   // warp-uniform: a warp's items are one row
+          load_fp4(S, list[ri], it[i]);
+          continue;
+        }
         if (ri < S.nsel) {
           const int64_t j = list[ri];
           b = S.sel_b + j * kDim;
@@ -305,10 +323,11 @@ __device__ __forceinline__ void load_step(const int *list, const Src &S, int row
 // column block, whose 16-byte chunk positions repeat the first block's, so
 // they store their upper half first and every phase touches 8 distinct
 // positions.  Rows at or past `valid_rows` (step-relative) are written as zeros.
-template <bool kMasked>
+template <bool kMasked, bool kFp4>
 __device__ __forceinline__ void store_step(uint8_t *R, int half, bool swap, int row0,
                                            const uint32_t (&off)[kItemsPerThread][2],
-                                           int64_t valid_rows, const Item (&it)[kItemsPerThread]) {
+                                           int64_t valid_rows, int64_t fp4_rows,
+                                           const Item (&it)[kItemsPerThread]) {
   uint8_t *Rb = R + half * (kStepRows / 8) * 1024;
 #pragma unroll
   for (int i = 0; i < kItemsPerThread; ++i) {
@@ -319,14 +338,31 @@ __device__ __forceinline__ void store_step(uint8_t *R, int half, bool swap, int 
         cd = make_uint4(0, 0, 0, 0);
         sc = 0.f;
       }
-      const __half2 s2 = __float2half2_rn(sc);
-      const uint32_t a = swap ? cd.z : cd.x, b = swap ? cd.w : cd.y;
-      const uint32_t c = swap ? cd.x : cd.z, d = swap ? cd.y : cd.w;
       uint32_t h[8];
-      e4m3x4_f16x4(a, h[0], h[1]);
-      e4m3x4_f16x4(b, h[2], h[3]);
-      e4m3x4_f16x4(c, h[4], h[5]);
-      e4m3x4_f16x4(d, h[6], h[7]);
+      __half2 s2;
+      if (kFp4 && row0 + i * kRowStride < fp4_rows) {
+        // E2M1 x E4M3 scale is exact in f16 (at most 5 significant bits,
+        // magnitudes in [2^-10, 2688])
+        uint32_t sl, sh;
+        e4m3x4_f16x4(cd.z | (cd.z << 8), sl, sh);
+        s2 = *reinterpret_cast<const __half2 *>(&sl);
+        uint32_t lo[4], hi[4];
+        e2m1x8_f16x8(swap ? cd.y : cd.x, lo);
+        e2m1x8_f16x8(swap ? cd.x : cd.y, hi);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          h[j] = lo[j];
+          h[4 + j] = hi[j];
+        }
+      } else {
+        s2 = __float2half2_rn(sc);
+        const uint32_t a = swap ? cd.z : cd.x, b = swap ? cd.w : cd.y;
+        const uint32_t c = swap ? cd.x : cd.z, d = swap ? cd.y : cd.w;
+        e4m3x4_f16x4(a, h[0], h[1]);
+        e4m3x4_f16x4(b, h[2], h[3]);
+        e4m3x4_f16x4(c, h[4], h[5]);
+        e4m3x4_f16x4(d, h[6], h[7]);
+      }
 #pragma unroll
       for (int j = 0; j < 8; ++j) h[j] = hmul2_u32(h[j], s2);
       *reinterpret_cast<uint4 *>(Rb + off[i][0]) = make_uint4(h[0], h[1], h[2], h[3]);
@@ -335,6 +371,7 @@ __device__ __forceinline__ void store_step(uint8_t *R, int half, bool swap, int 
   }
 }
 
+template <bool kFp4>
 __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms) {
   const int ptid = threadIdx.x - kProducerWarp0 * 32;
   const int lane = threadIdx.x & 31;
@@ -399,8 +436,15 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms) {
     S.nrows = S.nsel + ms->meta[ms_slot][1];
     const int64_t win_first = ms->meta[ms_slot][2];
     const int64_t kv0 = ms->meta[ms_slot][3];
-    S.sel_b = P.kv_fp8 + kv0 * kDim + seg * 16;
-    S.sel_s = P.kv_scale + kv0 * (kDim / 32) + seg / 2;
+    if (kFp4) {
+      S.sel_b = P.kv_fp8 + kv0 * (kDim / 2) + seg * 8;
+      S.sel_sf = P.kv_sf + kv0 * (kDim / 16) + seg;
+      S.sel_s = nullptr;
+    } else {
+      S.sel_b = P.kv_fp8 + kv0 * kDim + seg * 16;
+      S.sel_s = P.kv_scale + kv0 * (kDim / 32) + seg / 2;
+      S.sel_sf = nullptr;
+    }
     S.win_b = P.swa_fp8 + win_first * kDim + seg * 16;
     S.win_s = P.swa_scale + win_first * (kDim / 32) + seg / 2;
     S.dummy_b = P.swa_fp8 + seg * 16;
@@ -410,19 +454,20 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms) {
     // in flight while a step waits for its buffer and is stored
     const int nsteps = nch * 2;
     Item b0[kItemsPerThread], b1[kItemsPerThread];
-    load_step(list, S, row0, 0, b0);
+    load_step<kFp4>(list, S, row0, 0, b0);
     bool ok = true;
     // one step: prefetch step st+1 into `pre`, then store step st from `use`
     auto step = [&](int st, Item(&use)[kItemsPerThread], Item(&pre)[kItemsPerThread]) -> bool {
       const uint32_t gc = g + (uint32_t)(st >> 1), buf = gc & 1;
-      if (st + 1 < nsteps) load_step(list, S, row0, st + 1, pre);
+      if (st + 1 < nsteps) load_step<kFp4>(list, S, row0, st + 1, pre);
       if (!wait_bar(&ms->r_empty[buf], ((gc >> 1) & 1) ^ 1, ms)) return false;
       uint8_t *R = smem + kOffR + buf * kRBuf;
       const int64_t valid_rows = S.nrows - (int64_t)st * kStepRows;
+      const int64_t fp4_rows = S.nsel - (int64_t)st * kStepRows;
       if (valid_rows >= kStepRows)
-        store_step<false>(R, st & 1, swap, row0, off, valid_rows, use);
+        store_step<false, kFp4>(R, st & 1, swap, row0, off, valid_rows, fp4_rows, use);
       else
-        store_step<true>(R, st & 1, swap, row0, off, valid_rows, use);
+        store_step<true, kFp4>(R, st & 1, swap, row0, off, valid_rows, fp4_rows, use);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ms->r_full[buf]);
@@ -742,6 +787,7 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
   }
 }
 
+template <bool kFp4>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(Params P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Misc *ms = reinterpret_cast<Misc *>(smem + kOffMisc);
@@ -780,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(Params P) {
   } else if (warp == kOWarp) {
     o_issuer_role(P, smem, ms);
   } else {
-    producer_role(P, smem, ms);
+    producer_role<kFp4>(P, smem, ms);
   }
   fence_before_sync();
   __syncthreads();
@@ -806,21 +852,25 @@ int sm_count() {
 
 }  // namespace
 
-int attn_tc(const Batch &b, int n_heads, const __nv_bfloat16 *q, const uint8_t *kv_fp8,
-            const float *kv_scale, const int32_t *idx, int k, const uint8_t *swa_fp8,
+int attn_tc(const Batch &b, int n_heads, const __nv_bfloat16 *q, const uint8_t *kv_codes,
+            const float *kv_scale, const uint8_t *kv_sf, const int32_t *idx, int k,
+            const uint8_t *swa_fp8,
             const float *swa_scale, const int64_t *win_lo, int window, float sm_scale,
             const float *sink, __nv_bfloat16 *out, float *lse, int32_t *d_err,
             cudaStream_t st) {
   if (b.num_q == 0) return CSA2_OK;
   if (n_heads > kHeadsPad || k > kMaxSel) return CSA2_ERR_UNSUPPORTED;
   // 16-byte vector loads and asynchronous copies need 16-byte aligned rows
-  if (((uintptr_t)q | (uintptr_t)kv_fp8 | (uintptr_t)swa_fp8) & 15u) return CSA2_ERR_UNSUPPORTED;
+  // (FP4 main-KV rows are read 8 bytes at a time)
+  if (((uintptr_t)q | (uintptr_t)swa_fp8) & 15u) return CSA2_ERR_UNSUPPORTED;
+  if ((uintptr_t)kv_codes & (kv_sf ? 7u : 15u)) return CSA2_ERR_UNSUPPORTED;
   Params P;
   P.b = b;
   P.n_heads = n_heads;
   P.q = q;
-  P.kv_fp8 = kv_fp8;
+  P.kv_fp8 = kv_codes;
   P.kv_scale = kv_scale;
+  P.kv_sf = kv_sf;
   P.idx = idx;
   P.k = idx ? k : 0;
   P.swa_fp8 = swa_fp8;
@@ -832,10 +882,16 @@ int attn_tc(const Batch &b, int n_heads, const __nv_bfloat16 *q, const uint8_t *
   P.out = out;
   P.lse = lse;
   P.d_err = d_err;
-  cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)kSmemBytes);
   const int grid = b.num_q < sm_count() ? b.num_q : sm_count();
-  attn_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(P);
+  if (kv_sf) {
+    cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)kSmemBytes);
+    attn_tc_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(P);
+  } else {
+    cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)kSmemBytes);
+    attn_tc_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(P);
+  }
   return launch_status();
 }
 

@@ -118,19 +118,6 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, __half2 s) {
   return *reinterpret_cast<uint32_t *>(&x);
 }
 
-// four bytes of E2M1 code pairs -> four f16x2 (byte b -> h[b]; low nibble in
-// the low half); the bytes are taken apart by a vector move, not by shifts
-__device__ __forceinline__ void e2m1x8_f16x8(uint32_t w, uint32_t (&h)[4]) {
-  asm("{ .reg .b8 b0, b1, b2, b3;\n\t"
-      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-      : "r"(w));
-}
-
 // 32 E2M1 codes (16 bytes) times a power-of-two scale -> 32 f16 (4 x uint4)
 __device__ __forceinline__ void dequant32(const uint4 c, float scale, uint4 (&o)[4]) {
   const __half2 s2 = __float2half2_rn(scale);

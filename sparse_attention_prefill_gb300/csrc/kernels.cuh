@@ -14,8 +14,12 @@ int topk_launch(const Batch &b, const float *scores, int64_t ld, int k,
                 int32_t *count, int32_t *blocks_out, int32_t *nblocks_out, int32_t *d_err,
                 cudaStream_t st);
 
-int attn_tc(const Batch &b, int n_heads, const __nv_bfloat16 *q, const uint8_t *kv_fp8,
-            const float *kv_scale, const int32_t *idx, int k, const uint8_t *swa_fp8,
+// kv_sf == nullptr: selected rows are FP8 block-32 (kv_codes [Nkv,512] E4M3 +
+// kv_scale fp32 [Nkv,16]); otherwise FP4 (kv_codes [Nkv,256] E2M1 pairs +
+// kv_sf [Nkv,32] E4M3, one scale per 16 channels).  Window rows are FP8.
+int attn_tc(const Batch &b, int n_heads, const __nv_bfloat16 *q, const uint8_t *kv_codes,
+            const float *kv_scale, const uint8_t *kv_sf, const int32_t *idx, int k,
+            const uint8_t *swa_fp8,
             const float *swa_scale, const int64_t *win_lo, int window, float sm_scale,
             const float *sink, __nv_bfloat16 *out, float *lse, int32_t *d_err,
             cudaStream_t st);

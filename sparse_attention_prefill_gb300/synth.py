@@ -88,6 +88,26 @@ def encode_fp8_block32(x: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
     return codes.contiguous(), scale.reshape(*x.shape[:-1], d // 32).contiguous()
 
 
+def encode_fp4kv(x: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
+    """x [..., D] float32 -> (E2M1 codes uint8 [..., D/2], E4M3 scale codes
+    uint8 [..., D/16]): the main-KV FP4 layout, one E4M3 scale per 16 channels
+    (amax/6 rounded to E4M3, no second-level global scale), elements x/scale
+    clamped to +-6 and rounded to the E2M1 grid; element 2i in the low nibble."""
+    d = x.shape[-1]
+    g = x.reshape(*x.shape[:-1], d // 16, 16)
+    amax = g.abs().amax(-1, keepdim=True)
+    sc = (amax / 6.0).clamp(max=448.0).to(torch.float8_e4m3fn)
+    s = sc.to(torch.float32)
+    y = torch.where(s > 0, g / torch.where(s > 0, s, torch.ones_like(s)), torch.zeros_like(g))
+    y = y.clamp(-6.0, 6.0)
+    mid = torch.tensor(_E2M1_MID, device=x.device, dtype=torch.float32)
+    mag_code = torch.bucketize(y.abs(), mid).to(torch.uint8)
+    code = mag_code | ((y < 0) & (mag_code > 0)).to(torch.uint8) << 3
+    code = code.reshape(*x.shape[:-1], d)
+    packed = code[..., 0::2] | (code[..., 1::2] << 4)
+    return packed.contiguous(), sc.view(torch.uint8).reshape(*x.shape[:-1], d // 16).contiguous()
+
+
 def fp8_rows(n: int, seed: int, tensor_id: str, device, dim: int = DIM):
     """n N(0,1) rows encoded as E4M3 block-32 (generated in chunks)."""
     codes = torch.empty((n, dim), dtype=torch.uint8, device=device)
@@ -97,6 +117,17 @@ def fp8_rows(n: int, seed: int, tensor_id: str, device, dim: int = DIM):
         x = randn((c1 - c0, dim), seed, f"{tensor_id}/{c0}", device)
         codes[c0:c1], scales[c0:c1] = encode_fp8_block32(x)
     return codes, scales
+
+
+def fp4kv_rows(n: int, seed: int, tensor_id: str, device, dim: int = DIM):
+    """The same N(0,1) rows as fp8_rows(n, seed, tensor_id) in the FP4 main-KV layout."""
+    codes = torch.empty((n, dim // 2), dtype=torch.uint8, device=device)
+    sf = torch.empty((n, dim // 16), dtype=torch.uint8, device=device)
+    for c0 in range(0, n, _CHUNK_ROWS):
+        c1 = min(n, c0 + _CHUNK_ROWS)
+        x = randn((c1 - c0, dim), seed, f"{tensor_id}/{c0}", device)
+        codes[c0:c1], sf[c0:c1] = encode_fp4kv(x)
+    return codes, sf
 
 
 def fp4_rows(n: int, seed: int, tensor_id: str, device, dim: int = IDX_DIM):
@@ -123,6 +154,9 @@ class Pool:
     k_scale: torch.Tensor     # [Nkv, 4] f32
     kv_start: torch.Tensor    # [R] int64
     kv_len: torch.Tensor      # [R] int64
+    tag: str = ""             # generator stream of the rows
+    kv_fp4: Optional[torch.Tensor] = None   # [Nkv, 256] uint8 E2M1 (FP4 main-KV layout)
+    kv_sf: Optional[torch.Tensor] = None    # [Nkv, 32] uint8 E4M3 scale per 16 channels
 
 
 @dataclasses.dataclass
@@ -202,7 +236,16 @@ def make_pool(entries: List[int], seed: int, tag: str, device) -> Pool:
         s += int(n)
     kv_fp8, kv_scale = fp8_rows(s, seed, f"{tag}/kv", device)
     k_fp4, k_scale = fp4_rows(s, seed, f"{tag}/k", device)
-    return Pool(kv_fp8, kv_scale, k_fp4, k_scale, _i64(starts, device), _i64(entries, device))
+    return Pool(kv_fp8, kv_scale, k_fp4, k_scale, _i64(starts, device), _i64(entries, device),
+                tag)
+
+
+def with_fp4kv(w: "Workload", seed: int = 0) -> "Workload":
+    """Add the FP4 main-KV encoding of the workload's pool rows (the same
+    underlying N(0,1) rows as its FP8 pool)."""
+    p = w.pool
+    p.kv_fp4, p.kv_sf = fp4kv_rows(p.kv_fp8.shape[0], seed, f"{p.tag}/kv", p.kv_fp8.device)
+    return w
 
 
 def make_layer(name: str, mode: str, nq: int, n_heads: int, n_idx_heads: int,
