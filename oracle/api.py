@@ -38,7 +38,8 @@ def lib():
         _lib.oracle_n_visible.argtypes = [C.c_int64, C.c_int]
         for name in ("oracle_tail_layout", "oracle_index_score", "oracle_topk",
                      "oracle_topk_candidates", "oracle_sparse_swa_attn",
-                     "oracle_sparse_swa_attn_fp4kv"):
+                     "oracle_sparse_swa_attn_fp4kv", "oracle_encoder_replay_layout",
+                     "oracle_rows_gather", "oracle_rows_scatter"):
             getattr(_lib, name).restype = C.c_int
         _lib.oracle_decode_fp4kv_row.restype = None
     return _lib
@@ -110,6 +111,51 @@ def tail_layout(extend_len, seq_len, window=128, capacity=None):
     n = min(int(cu_tail[-1]), int(capacity))
     return dict(tail_len=tail_len, cu_tail=cu_tail, src_row=src_row[:n], pos=pos[:n],
                 win_lo=win_lo[:n], row_req=row_req[:n]), err
+
+
+def encoder_replay_layout(prefix_len, extend_len, window=128, ratio=2, capacity=None):
+    p = _c(prefix_len, np.int64)
+    e = _c(extend_len, np.int32)
+    r = p.shape[0]
+    if capacity is None:
+        capacity = int(sum(min(window, max(int(a), 0)) + max(int(b), 0) for a, b in zip(p, e)))
+    replay_len = np.zeros(r, np.int32)
+    cu_rows = np.zeros(r + 1, np.int32)
+    cap = max(int(capacity), 1)
+    src_row = np.full(cap, -2, np.int32)
+    pos = np.full(cap, -1, np.int64)
+    win_lo = np.full(cap, -1, np.int64)
+    row_req = np.full(cap, -1, np.int32)
+    entry_range = np.zeros((max(r, 1), 2), np.int64)
+    err = lib().oracle_encoder_replay_layout(C.c_int32(r), _p(p), _p(e), C.c_int32(window),
+                                             C.c_int32(ratio), _p(replay_len), _p(cu_rows),
+                                             _p(src_row), _p(pos), _p(win_lo), _p(row_req),
+                                             _p(entry_range), C.c_int64(capacity))
+    n = min(int(cu_rows[-1]), int(capacity))
+    return dict(replay_len=replay_len, cu_rows=cu_rows, src_row=src_row[:n], pos=pos[:n],
+                win_lo=win_lo[:n], row_req=row_req[:n], entry_range=entry_range[:r]), err
+
+
+def rows_gather(row_idx, src, dst):
+    """dst[i] = src[row_idx[i]] (rows = leading axis); returns (new dst, err)."""
+    idx = _c(row_idx, np.int32)
+    s = np.ascontiguousarray(src)
+    d = np.array(dst, copy=True, order="C")
+    rb = int(s[0].nbytes) if s.shape[0] else int(d[0].nbytes)
+    err = lib().oracle_rows_gather(C.c_int64(idx.shape[0]), _p(idx), _p(s),
+                                   C.c_int64(s.shape[0]), _p(d), C.c_int64(rb))
+    return d, err
+
+
+def rows_scatter(row_idx, src, dst):
+    """dst[row_idx[i]] = src[i]; rows not named keep their values."""
+    idx = _c(row_idx, np.int32)
+    s = np.ascontiguousarray(src)
+    d = np.array(dst, copy=True, order="C")
+    rb = int(d[0].nbytes) if d.shape[0] else 0
+    err = lib().oracle_rows_scatter(C.c_int64(idx.shape[0]), _p(idx), _p(s), _p(d),
+                                    C.c_int64(d.shape[0]), C.c_int64(rb))
+    return d, err
 
 
 def index_score(b, q_fp4, q_scale, head_w, k_fp4, k_scale, ld,

@@ -34,6 +34,16 @@
  *                    block score = max score in the block, at most 2048 blocks,
  *                    the block holding the latest position always kept; the
  *                    filter excludes nothing when every reachable position fits.
+ *   encoder replay   "DeepSeek V4.1 Flash 建模", Encoder Bounded Replay card;
+ *                    article sec. 4.1 and 4.3: on a prefix hit whose SWA state
+ *                    is gone, the last 128 cached tokens are processed again
+ *                    with the new suffix; they rebuild SWA only, the cached
+ *                    global entries are read and never rewritten, and local
+ *                    attention is cut at the rebuild boundary.
+ *   row cut/restore  tail page sec. 2.2 and 2.7: the per-row state entering
+ *                    the late layers is cut to the tail rows, and the computed
+ *                    tail rows are scattered back into the full extend layout
+ *                    (the other rows are left as they were).
  *   attention        article sec. 1: each query attends to its own 128-token
  *                    window and to at most 512 selected compressed positions;
  *                    one softmax over both sets; the 512-dim latent row is both
@@ -55,7 +65,8 @@ enum {
   OR_ERR_SCALE = 8,
   OR_ERR_LD = 16,
   OR_ERR_CAPACITY = 32,
-  OR_ERR_BAD_EXTEND = 64
+  OR_ERR_BAD_EXTEND = 64,
+  OR_ERR_RANGE_ROW = 256
 };
 
 typedef struct {
@@ -189,6 +200,103 @@ int oracle_tail_layout(int32_t num_req, const int32_t *extend_len,
     if (e > 0) cu_e += e;
     cu_t += t;
     cu_tail[r + 1] = (int32_t)cu_t;
+  }
+  return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* encoder-side bounded replay layout                                         */
+/* ------------------------------------------------------------------------ */
+
+/* Per request r with P_r cached prefix tokens (global entries and index keys
+ * cached, SWA state gone) and E_r new tokens: the replayed part is the last
+ * Rp_r = min(W, P_r) cached tokens, so the rows processed are the positions
+ * P_r - Rp_r ... P_r + E_r - 1 in order.  A replayed row has no row in the
+ * packed new-token input (src_row = -1); new row k - Rp_r of the request sits
+ * at cu_E[r] + k - Rp_r.  Every row carries the window lower bound P_r - Rp_r
+ * (local attention is cut where the rebuild starts).  Global entries: with m
+ * tokens per entry, entry j is complete once token m*j + m - 1 exists, so the
+ * cache already holds entries j < floor(P_r / m) and this extend completes
+ * entries floor(P_r / m) <= j < floor((P_r + E_r) / m): entry_range[2r] and
+ * entry_range[2r+1].  Returns the OR of data-error bits. */
+int oracle_encoder_replay_layout(int32_t num_req, const int64_t *prefix_len,
+                                 const int32_t *extend_len, int32_t window, int32_t ratio,
+                                 int32_t *replay_len, int32_t *cu_rows, int32_t *src_row,
+                                 int64_t *pos, int64_t *win_lo, int32_t *row_req,
+                                 int64_t *entry_range, int64_t capacity) {
+  int err = 0;
+  int64_t cu_e = 0, cu_n = 0;
+  cu_rows[0] = 0;
+  for (int r = 0; r < num_req; ++r) {
+    int64_t p = prefix_len[r], e = extend_len[r];
+    int64_t rp = 0, n = 0;
+    if (p < 0 || e < 0) {
+      err |= OR_ERR_BAD_EXTEND;
+      p = 0;
+      e = 0;
+    } else {
+      rp = p < window ? p : window;
+      n = rp + e;
+    }
+    replay_len[r] = (int32_t)rp;
+    if (entry_range) {
+      entry_range[2 * r] = p / ratio;
+      entry_range[2 * r + 1] = (p + e) / ratio;
+    }
+    for (int64_t k = 0; k < n; ++k) {
+      int64_t row = cu_n + k;
+      if (row >= capacity) {
+        err |= OR_ERR_CAPACITY;
+        continue;
+      }
+      pos[row] = p - rp + k;
+      win_lo[row] = p - rp;
+      src_row[row] = k < rp ? -1 : (int32_t)(cu_e + (k - rp));
+      if (row_req) row_req[row] = r;
+    }
+    cu_e += e;
+    cu_n += n;
+    cu_rows[r + 1] = (int32_t)cu_n;
+  }
+  return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* row cut (gather) and scatter-back                                          */
+/* ------------------------------------------------------------------------ */
+
+/* dst row i = src row row_idx[i] for i < n (rows of row_bytes bytes).  A
+ * negative index leaves dst row i as it was; an index >= src_rows does too and
+ * sets the RANGE_ROW bit. */
+int oracle_rows_gather(int64_t n, const int32_t *row_idx, const uint8_t *src, int64_t src_rows,
+                       uint8_t *dst, int64_t row_bytes) {
+  int err = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    int64_t j = row_idx[i];
+    if (j < 0) continue;
+    if (j >= src_rows) {
+      err |= OR_ERR_RANGE_ROW;
+      continue;
+    }
+    memcpy(dst + i * row_bytes, src + j * row_bytes, (size_t)row_bytes);
+  }
+  return err;
+}
+
+/* dst row row_idx[i] = src row i for i < n; the dst rows no index names are
+ * left as they were.  Negative indices are skipped; indices >= dst_rows are
+ * skipped and set the RANGE_ROW bit. */
+int oracle_rows_scatter(int64_t n, const int32_t *row_idx, const uint8_t *src, uint8_t *dst,
+                        int64_t dst_rows, int64_t row_bytes) {
+  int err = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    int64_t j = row_idx[i];
+    if (j < 0) continue;
+    if (j >= dst_rows) {
+      err |= OR_ERR_RANGE_ROW;
+      continue;
+    }
+    memcpy(dst + j * row_bytes, src + i * row_bytes, (size_t)row_bytes);
   }
   return err;
 }

@@ -121,3 +121,33 @@ def test_bad_extend_and_capacity_flags():
     out, err = O.tail_layout(np.array([200, 200]), np.array([200, 300]), 128, capacity=150)
     assert err & 32
     assert out["cu_tail"].tolist() == [0, 128, 256]
+
+
+@pytest.mark.parametrize("R", [64, 256, 512])
+def test_replay_budget_sweep(R):
+    """"SGLang 如何让 DeepSeek V4.1 Flash 的后半层只处理尾部 token", sec. 3.5: the
+    rows kept (R) are swept while the SWA width stays 128.  The layout keeps
+    T = min(R, E) rows per request with lower bound S - T, and a kept row at t
+    reads the positions [max(S - T, t - 127), t]: for R > 128 the first 127
+    rows of a tail are cut by the bound, the rest see a full window."""
+    es, ss = [8192, 100, 1000], [8192, 600, 5000]
+    out = _tail(es, ss, R)
+    ts = [min(R, e) for e in es]
+    assert out["tail_len"].tolist() == ts
+    cu_e = np.concatenate([[0], np.cumsum(es)])
+    rows, pos, lo = [], [], []
+    for r, (e, s, t) in enumerate(zip(es, ss, ts)):
+        rows += [int(cu_e[r]) + e - t + k for k in range(t)]
+        pos += [s - t + k for k in range(t)]
+        lo += [s - t] * t
+    assert out["src_row"].tolist() == rows
+    assert out["pos"].tolist() == pos
+    assert out["win_lo"].tolist() == lo
+    # windows of the first request's rows (S = E = 8192)
+    s, t = 8192, ts[0]
+    for k in sorted({0, 1, 126, 127, 128, t - 1} & set(range(t))):
+        q = s - t + k
+        count, mean = _window_rows_used(q, s - t)
+        first = max(s - t, q - 127)
+        assert count == q - first + 1 == min(k + 1, 128)
+        assert abs(mean - (first + q) / 2) <= 2 ** -8 * abs(mean)
