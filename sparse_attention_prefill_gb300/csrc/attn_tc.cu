@@ -82,7 +82,7 @@ constexpr int kDerrTimeout = 128;
 
 struct Misc {
   uint64_t q_full, q_empty, o_full, o_empty, done, done_o, sm_grp;
-  uint64_t r_full[2], r_empty[2], s_full[2], s_empty[2], p_full[2], p_empty[2];
+  uint64_t r_full[2], r_empty[2][2], s_full[2], s_empty[2], p_full[2], p_empty[2];
   uint64_t meta_full[2];
   int64_t meta[2][4];   // per query (ring of 2): selected rows, window rows, first SWA
                         // row, pool row of the request's entry 0
@@ -460,7 +460,7 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms) {
     auto step = [&](int st, Item(&use)[kItemsPerThread], Item(&pre)[kItemsPerThread]) -> bool {
       const uint32_t gc = g + (uint32_t)(st >> 1), buf = gc & 1;
       if (st + 1 < nsteps) load_step<kFp4>(list, S, row0, st + 1, pre);
-      if (!wait_bar(&ms->r_empty[buf], ((gc >> 1) & 1) ^ 1, ms)) return false;
+      if (!wait_bar(&ms->r_empty[buf][st & 1], ((gc >> 1) & 1) ^ 1, ms)) return false;
       uint8_t *R = smem + kOffR + buf * kRBuf;
       const int64_t valid_rows = S.nrows - (int64_t)st * kStepRows;
       const int64_t fp4_rows = S.nsel - (int64_t)st * kStepRows;
@@ -553,7 +553,7 @@ __device__ void s_issuer_role(const Params &P, uint8_t *smem, Misc *ms) {
 
 // O^T issuer (lane 0 of warp kOWarp): O^T += R(g)^T . P(g)^T as soon as P(g) is
 // written.  S^T(g) has completed by then (the softmax read it), so this
-// issuer's commit releases R(g) for both products.
+// issuer's commits release R(g), half by half, for both products.
 __device__ void o_issuer_role(const Params &P, uint8_t *smem, Misc *ms) {
   const int lane = threadIdx.x & 31;
   if (lane == 0) {
@@ -573,16 +573,21 @@ __device__ void o_issuer_role(const Params &P, uint8_t *smem, Misc *ms) {
         if (!ok) break;
         fence_after_sync();
         const uint32_t ra = D.rm_lo + ((buf * kRBuf) >> 4), pa = D.p_lo + ((buf * kPBuf) >> 4);
+        // rows 0-31 of the chunk first, so the producers can refill that half
+        // while the second half is still being read
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
+        for (int half = 0; half < 2; ++half) {
 #pragma unroll
-          for (int ks = 0; ks < kChunk / 16; ++ks) {
-            mma_f16_split(tmem + kColO + t * 64, ra + ((t * 2 * kRBlock + ks * 2048) >> 4),
-                          D.rm_hi, pa + ((ks * 2048) >> 4), D.p_hi, id_o,
-                          (c > 0 || ks > 0) ? 1u : 0u);
+          for (int t = 0; t < 4; ++t) {
+#pragma unroll
+            for (int ks = 2 * half; ks < 2 * half + 2; ++ks) {
+              mma_f16_split(tmem + kColO + t * 64, ra + ((t * 2 * kRBlock + ks * 2048) >> 4),
+                            D.rm_hi, pa + ((ks * 2048) >> 4), D.p_hi, id_o,
+                            (c > 0 || ks > 0) ? 1u : 0u);
+            }
           }
+          mma_commit(&ms->r_empty[buf][half]);
         }
-        mma_commit(&ms->r_empty[buf]);
         mma_commit(&ms->p_empty[buf]);
         if (c == nch - 1) mma_commit(&ms->o_full);
       }
@@ -802,7 +807,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(Params P) {
     mbar_init(&ms->sm_grp, kSoftmaxWarps);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ms->r_full[i], 2 * kProducerWarps);   // two steps per chunk
-      mbar_init(&ms->r_empty[i], 1);
+      mbar_init(&ms->r_empty[i][0], 1);
+      mbar_init(&ms->r_empty[i][1], 1);
       mbar_init(&ms->s_full[i], 1);
       mbar_init(&ms->s_empty[i], kSoftmaxWarps);
       mbar_init(&ms->p_full[i], kSoftmaxWarps);
