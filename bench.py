@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-fp4kv", action="store_true",
                     help="skip the FP4 main-KV attention measurement")
+    ap.add_argument("--no-rows", action="store_true",
+                    help="skip the tail cut / scatter-back measurement")
     ap.add_argument("--no-cpu", action="store_true")
     return ap.parse_args()
 
@@ -225,13 +227,15 @@ def bench_ours(args, rank, world, local_rank):
                 "share_of_step": round(sum(attn_ms) / sum(step_ms), 3)}
 
     fp4 = None if args.no_fp4kv else bench_fp4kv(args, w, run, stream, flush, hbm)
+    cut = None if args.no_rows else bench_rows(args, w, run, stream, flush, hbm)
 
     e2e = None
     if not args.no_e2e:
         e2e = bench_e2e(args, w, run, dev, rank, world)
 
     return dict(value=value, ms=ms, wall=wall, clocks=clk, roofline=roofline, e2e=e2e,
-                launches=launches_per_step * args.steps, rows=rows, w=w, fp4kv=fp4)
+                launches=launches_per_step * args.steps, rows=rows, w=w, fp4kv=fp4,
+                rows_copy=cut)
 
 
 def bench_fp4kv(args, w, run, stream, flush, hbm):
@@ -267,6 +271,54 @@ def bench_fp4kv(args, w, run, stream, flush, hbm):
             "avg_launch_ms": round(ms, 4), "algorithmic_bytes_per_launch": int(byts),
             "achieved_gbs": round(byts / (ms * 1e-3) / 1e9, 1), "peak_gbs": hbm,
             "frac": round(byts / (ms * 1e-3) / 1e9 / hbm, 4)}
+
+
+MHC_STREAMS, HIDDEN = 4, 5120     # V4.1: n = 4 residual streams of hidden size 5120
+
+
+def bench_rows(args, w, run, stream, flush, hbm):
+    """The cut of the per-row mHC state (4 streams x 5120 bf16 = 40 KB per row)
+    of the 8 x 8192-row extend to its 1024 tail rows, and the scatter-back of
+    the tail rows into the full extend layout, both driven by the tail layout's
+    src_row with the row count read on the device.  Timed per launch with
+    events, L2 flushed between launches."""
+    import torch
+    import sparse_attention_prefill_gb300 as S
+    dev = w.q_pos.device
+    n_full = int(w.extend_len.sum().item())
+    row_bytes = MHC_STREAMS * HIDDEN * 2
+    full = torch.empty((n_full, MHC_STREAMS * HIDDEN), dtype=torch.bfloat16, device=dev)
+    full.normal_()
+    t = run.tail
+    cap = t["src_row"].shape[0]
+    cut = torch.empty((cap, MHC_STREAMS * HIDDEN), dtype=torch.bfloat16, device=dev)
+    count = t["cu_tail"][-1:]
+    res = {}
+    for name, fn in (("gather", lambda: S.rows_gather(t["src_row"], full, cut, count=count,
+                                                      d_err=run.d_err)),
+                     ("scatter", lambda: S.rows_scatter(t["src_row"], cut, full, count=count,
+                                                        d_err=run.d_err))):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(max(5, min(args.steps, 20))):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in ts) / len(ts)
+        n = run.nq
+        byts = 2 * n * row_bytes + 4 * n
+        res[name] = {"avg_launch_ms": round(ms, 4), "algorithmic_bytes_per_launch": int(byts),
+                     "achieved_gbs": round(byts / (ms * 1e-3) / 1e9, 1),
+                     "frac": round(byts / (ms * 1e-3) / 1e9 / hbm, 4)}
+    assert int(run.d_err.item()) == 0
+    return {"kernel": "csa2_rows_gather / csa2_rows_scatter",
+            "rows": f"{run.nq} tail rows of {n_full}, {row_bytes} B each (mHC state)",
+            "peak_gbs": hbm, **res}
 
 
 def run_kernel_id():
@@ -372,7 +424,7 @@ def oracle_sample_step(w, rows_per_req, threads):
     O.set_threads(threads)
     npy = lambda t: None if t is None else (t.cpu().view(torch.int16).numpy().view(np.uint16)
                                             if t.dtype == torch.bfloat16 else t.cpu().numpy())
-    tail, _ = O.tail_layout(npy(w.extend_len), npy(w.seq_len), w.window)
+    tail, _ = O.tail_layout(npy(w.extend_len), npy(w.seq_len), w.replay)
     sel = np.concatenate([np.arange(tail["cu_tail"][r + 1] - rows_per_req, tail["cu_tail"][r + 1])
                           for r in range(w.num_req)])
     rows = torch.from_numpy(sel)
@@ -493,7 +545,8 @@ def main():
                 "config": config_block(r["w"], {"parallelism": "replicas" if world > 1 else "1gpu"}),
                 "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r["e2e"],
                 "clocks": r["clocks"], "gpu_launches": r["launches"],
-                "wall_s_timed_region": round(r["wall"], 4), "fp4_kv_attention": r["fp4kv"]}
+                "wall_s_timed_region": round(r["wall"], 4), "fp4_kv_attention": r["fp4kv"],
+                "tail_cut_restore": r["rows_copy"]}
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

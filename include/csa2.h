@@ -72,6 +72,7 @@ typedef struct CUstream_st *csa2_stream_t; /* same object as cudaStream_t */
 #define CSA2_DERR_CAPACITY 32     /* tail rows beyond the output capacity */
 #define CSA2_DERR_BAD_EXTEND 64   /* an extend with E < 0 or S < E */
 #define CSA2_DERR_TIMEOUT 128     /* a pipeline wait inside a kernel gave up (internal error) */
+#define CSA2_DERR_RANGE_ROW 256   /* a row index past the rows of a gather source / scatter target */
 
 /* Rows of one layer call.  Host struct; every array is device memory.
  *   q_req[Nq]   request of each query row (0 <= q_req < num_req)
@@ -255,6 +256,67 @@ CSA2_API int csa2_sparse_swa_attn_fp4kv(const csa2_batch *b, int32_t n_heads, in
                          const int64_t *win_lo, int32_t window, float sm_scale,
                          const float *sink, void *out_bf16, float *lse,
                          int32_t *d_err, csa2_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Encoder-side bounded replay layout   [CSA2] Encoder Bounded Replay card
+ * ("只重放已缓存前缀的最近 128 token，再继续处理新后缀"; replayed tokens only
+ * regenerate SWA KV and never overwrite the cached global KV); [D0] sec. 4.1
+ * and 4.3 (local attention is cut at the rebuild boundary).
+ *
+ * For each request r with P_r = prefix_len[r] cached tokens (global entries
+ * and index keys cached, SWA state gone) and E_r = extend_len[r] new tokens,
+ * Rp_r = min(window, P_r) cached tokens are processed again before the new
+ * ones:
+ *   replay_len[r] = Rp_r                                            [R]
+ *   cu_rows[r]    = sum over r' < r of (Rp_r' + E_r'); cu_rows[R] = total
+ *   for k < Rp_r + E_r, row i = cu_rows[r] + k:
+ *     pos[i]     = P_r - Rp_r + k      (absolute position)
+ *     win_lo[i]  = P_r - Rp_r          (window lower bound for attention)
+ *     src_row[i] = -1 for k < Rp_r     (a replayed cached token; no input row)
+ *                  cu_E[r] + k - Rp_r  (row in the packed new-token input)
+ *     row_req[i] = r                   (optional; may be NULL)
+ *   entry_range[2r], entry_range[2r+1] (optional; may be NULL) =
+ *     floor(P_r / ratio), floor((P_r + E_r) / ratio): the global entries this
+ *     extend completes and writes.  Entries below the first are cached and
+ *     only read; with ratio 2 and P_r odd the first new entry pairs the last
+ *     cached token (a replayed row) with the first new one.
+ * With Rp_r = 128 every new row's 128-token window lies inside the rebuilt
+ * rows, so only replayed rows see a cut window.  ratio in {1, 2}; window >= 1.
+ * Rows at or beyond `capacity` are not written (CSA2_DERR_CAPACITY).  P_r < 0
+ * or E_r < 0 gives no rows for r, entry range [0, 0) and CSA2_DERR_BAD_EXTEND.
+ * ------------------------------------------------------------------------- */
+CSA2_API int csa2_encoder_replay_layout(int32_t num_req, const int64_t *prefix_len,
+                         const int32_t *extend_len, int32_t window, int32_t ratio,
+                         int32_t *replay_len, int32_t *cu_rows, int32_t *src_row,
+                         int64_t *pos, int64_t *win_lo, int32_t *row_req,
+                         int64_t *entry_range, int64_t capacity, int32_t *d_err,
+                         csa2_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Row cut and scatter-back   [TAIL] sec. 2.2 (entering the late layers the
+ * per-row state is cut to the tail rows; the outer layout is restored after
+ * them) and sec. 2.7 (the computed tail rows are scattered back into the full
+ * extend layout; the other rows are not filled in and must not be read).
+ *
+ * Rows are `row_bytes` bytes (a multiple of 16; src and dst 16-byte aligned,
+ * not overlapping).  The rows processed are i < n, with n = *count read on
+ * the device (e.g. cu_tail + num_req written by csa2_tail_layout, so no host
+ * sync is needed), capped at `capacity`; count == NULL means n = capacity.
+ *   gather:  dst row i          = src row row_idx[i]   (the cut)
+ *   scatter: dst row row_idx[i] = src row i            (the scatter-back)
+ * A negative row_idx[i] skips row i (the encoder layout's replayed rows); an
+ * index >= src_rows (gather) or >= dst_rows (scatter) skips it and sets
+ * CSA2_DERR_RANGE_ROW.  Rows of dst that are not written keep their bytes.
+ * Scatter indices are expected to be distinct (a layout's src_row is).
+ * ------------------------------------------------------------------------- */
+CSA2_API int csa2_rows_gather(const int32_t *count, int64_t capacity,
+                         const int32_t *row_idx, const void *src, int64_t src_rows,
+                         void *dst, int64_t row_bytes, int32_t *d_err,
+                         csa2_stream_t stream);
+CSA2_API int csa2_rows_scatter(const int32_t *count, int64_t capacity,
+                         const int32_t *row_idx, const void *src, void *dst,
+                         int64_t dst_rows, int64_t row_bytes, int32_t *d_err,
+                         csa2_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -23,9 +23,11 @@ LIB_PATH = os.path.join(_HERE, "_build", "libcsa2.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 DERR_RANGE_IDX, DERR_RANGE_WINDOW, DERR_RANGE_CTX = 1, 2, 4
 DERR_SCALE, DERR_LD, DERR_CAPACITY, DERR_BAD_EXTEND = 8, 16, 32, 64
+DERR_TIMEOUT, DERR_RANGE_ROW = 128, 256
 
 EXPORTED = ("csa2_status_string", "csa2_tail_layout", "csa2_index_score", "csa2_topk",
-            "csa2_topk_candidates", "csa2_sparse_swa_attn", "csa2_sparse_swa_attn_fp4kv")
+            "csa2_topk_candidates", "csa2_sparse_swa_attn", "csa2_sparse_swa_attn_fp4kv",
+            "csa2_encoder_replay_layout", "csa2_rows_gather", "csa2_rows_scatter")
 
 
 class Csa2Error(RuntimeError):
@@ -64,6 +66,10 @@ def load(path: Optional[str] = None):
     lib.csa2_sparse_swa_attn.argtypes = [vp, i32, i32, vp, vp, vp, vp, i32, vp, vp, vp, i32, f32,
                                          vp, vp, vp, vp, vp]
     lib.csa2_sparse_swa_attn_fp4kv.argtypes = lib.csa2_sparse_swa_attn.argtypes
+    lib.csa2_encoder_replay_layout.argtypes = [i32, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp,
+                                               i64, vp, vp]
+    lib.csa2_rows_gather.argtypes = [vp, i64, vp, vp, i64, vp, i64, vp, vp]
+    lib.csa2_rows_scatter.argtypes = [vp, i64, vp, vp, vp, i64, i64, vp, vp]
     for name in EXPORTED[1:]:
         getattr(lib, name).restype = C.c_int
     _lib = lib
@@ -167,6 +173,29 @@ def csa2_sparse_swa_attn_fp4kv(batch, n_heads, dim, q_bf16, kv_fp4, kv_sf, idx, 
 
 
 # ---------------------------------------------------------------------------
+def csa2_encoder_replay_layout(num_req, prefix_len, extend_len, window, ratio, replay_len,
+                               cu_rows, src_row, pos, win_lo, row_req, entry_range, capacity,
+                               d_err, stream=None) -> int:
+    return load().csa2_encoder_replay_layout(
+        int(num_req), _ptr(prefix_len), _ptr(extend_len), int(window), int(ratio),
+        _ptr(replay_len), _ptr(cu_rows), _ptr(src_row), _ptr(pos), _ptr(win_lo), _ptr(row_req),
+        _ptr(entry_range), int(capacity), _ptr(d_err), _stream(stream))
+
+
+def csa2_rows_gather(count, capacity, row_idx, src, src_rows, dst, row_bytes, d_err,
+                     stream=None) -> int:
+    return load().csa2_rows_gather(_ptr(count), int(capacity), _ptr(row_idx), _ptr(src),
+                                   int(src_rows), _ptr(dst), int(row_bytes), _ptr(d_err),
+                                   _stream(stream))
+
+
+def csa2_rows_scatter(count, capacity, row_idx, src, dst, dst_rows, row_bytes, d_err,
+                      stream=None) -> int:
+    return load().csa2_rows_scatter(_ptr(count), int(capacity), _ptr(row_idx), _ptr(src),
+                                    _ptr(dst), int(dst_rows), int(row_bytes), _ptr(d_err),
+                                    _stream(stream))
+
+
 # allocating conveniences (torch allocates the outputs; the library computes)
 # ---------------------------------------------------------------------------
 
@@ -184,6 +213,47 @@ def tail_layout(extend_len, seq_len, window=128, d_err=None, stream=None):
                             out["src_row"], out["pos"], out["win_lo"], out["row_req"], r * window,
                             d_err, stream), "csa2_tail_layout")
     return out
+
+
+def encoder_replay_layout(prefix_len, extend_len, capacity, window=128, ratio=2, d_err=None,
+                          stream=None):
+    """Rows of an encoder extend over a cached prefix whose SWA state is gone:
+    the last min(window, P) cached positions replayed, then the new ones.
+    ``capacity`` bounds the rows written (sum of min(window, P) + E suffices)."""
+    r = int(prefix_len.shape[0])
+    dev = prefix_len.device
+    cap = max(1, int(capacity))
+    out = dict(replay_len=torch.empty(r, dtype=torch.int32, device=dev),
+               cu_rows=torch.empty(r + 1, dtype=torch.int32, device=dev),
+               src_row=torch.empty(cap, dtype=torch.int32, device=dev),
+               pos=torch.empty(cap, dtype=torch.int64, device=dev),
+               win_lo=torch.empty(cap, dtype=torch.int64, device=dev),
+               row_req=torch.empty(cap, dtype=torch.int32, device=dev),
+               entry_range=torch.empty((max(r, 1), 2), dtype=torch.int64, device=dev))
+    _check(csa2_encoder_replay_layout(r, prefix_len, extend_len, window, ratio,
+                                      out["replay_len"], out["cu_rows"], out["src_row"],
+                                      out["pos"], out["win_lo"], out["row_req"],
+                                      out["entry_range"], int(capacity), d_err, stream),
+           "csa2_encoder_replay_layout")
+    return out
+
+
+def rows_gather(row_idx, src, dst, count=None, d_err=None, stream=None):
+    """dst[i] = src[row_idx[i]] for i < count (device scalar) or len(row_idx);
+    negative indices leave dst[i] as it was."""
+    rb = src[0].numel() * src.element_size() if src.shape[0] else 0
+    _check(csa2_rows_gather(count, int(row_idx.shape[0]), row_idx, src, int(src.shape[0]), dst,
+                            rb, d_err, stream), "csa2_rows_gather")
+    return dst
+
+
+def rows_scatter(row_idx, src, dst, count=None, d_err=None, stream=None):
+    """dst[row_idx[i]] = src[i] for i < count or len(row_idx); rows of dst
+    that no index names keep their values."""
+    rb = dst[0].numel() * dst.element_size() if dst.shape[0] else 0
+    _check(csa2_rows_scatter(count, int(row_idx.shape[0]), row_idx, src, dst, int(dst.shape[0]),
+                             rb, d_err, stream), "csa2_rows_scatter")
+    return dst
 
 
 def index_score(batch, q_fp4, q_scale, head_w, k_fp4, k_scale, ld, cand_blocks=None, block=8,

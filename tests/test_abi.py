@@ -55,3 +55,22 @@ def test_product_package_does_not_use_the_oracle():
                 txt = open(os.path.join(dirpath, f), encoding="utf8").read()
                 assert not re.search(r"^\s*(from|import)\s+oracle", txt, re.M), f
                 assert "csa2_oracle" not in txt, f
+
+
+def test_host_validation_of_replay_and_row_calls():
+    from sparse_attention_prefill_gb300 import build
+    lib = ctypes.CDLL(build.build())
+    i64 = ctypes.c_int64
+    # negative request count; ratio outside {1, 2}
+    assert lib.csa2_encoder_replay_layout(-1, None, None, 128, 2, None, None, None, None, None,
+                                          None, None, i64(0), None, None) == 1
+    assert lib.csa2_encoder_replay_layout(0, None, None, 128, 3, None, None, None, None, None,
+                                          None, None, i64(0), None, None) == 1
+    # missing row map; nothing to copy; a row size that is not a multiple of 16
+    assert lib.csa2_rows_gather(None, i64(4), None, None, i64(0), None, i64(16), None,
+                                None) == 1
+    assert lib.csa2_rows_scatter(None, i64(0), None, None, None, i64(0), i64(16), None,
+                                 None) == 0
+    fake = ctypes.c_void_p(4096)
+    assert lib.csa2_rows_gather(None, i64(4), fake, fake, i64(8), fake, i64(24), None,
+                                None) == 2
