@@ -70,7 +70,7 @@ class LayerRunner:
         w = self.w
         r = w.num_req
         if self.tail is None:
-            cap = r * w.window
+            cap = r * w.replay
             self.tail = dict(tail_len=torch.empty(r, dtype=torch.int32, device=self.dev),
                              cu_tail=torch.empty(r + 1, dtype=torch.int32, device=self.dev),
                              src_row=torch.empty(cap, dtype=torch.int32, device=self.dev),
@@ -78,8 +78,10 @@ class LayerRunner:
                              win_lo=torch.empty(cap, dtype=torch.int64, device=self.dev),
                              row_req=torch.empty(cap, dtype=torch.int32, device=self.dev))
         t = self.tail
-        _check(csa2_tail_layout(r, w.extend_len, w.seq_len, w.window, t["tail_len"], t["cu_tail"],
-                                t["src_row"], t["pos"], t["win_lo"], t["row_req"], r * w.window,
+        # the tail keeps R = w.replay rows per request; attention keeps the SWA
+        # width w.window
+        _check(csa2_tail_layout(r, w.extend_len, w.seq_len, w.replay, t["tail_len"], t["cu_tail"],
+                                t["src_row"], t["pos"], t["win_lo"], t["row_req"], r * w.replay,
                                 self.d_err), "csa2_tail_layout")
         return t
 

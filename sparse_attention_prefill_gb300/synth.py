@@ -189,6 +189,7 @@ class Workload:
     layers: Dict[str, Layer]
     topk: int = TOPK
     window: int = WINDOW
+    replay: int = WINDOW       # rows kept per request by the tail layout (R)
     block: int = BLOCK
     max_blocks: int = MAX_BLOCKS
     extend_len: Optional[torch.Tensor] = None   # [R] int32 when the rows are tails
@@ -293,18 +294,21 @@ def full_layer(ctx: int, ratio: int, q_positions: List[int], n_heads: int, n_idx
 
 def decoder_replay(extends: List[int], prefixes: List[int], n_heads: int, n_idx_heads: int,
                    seed: int = 0, device="cpu", tag: str = "replay",
-                   topk: int = TOPK, max_blocks: int = MAX_BLOCKS, block: int = BLOCK) -> Workload:
+                   topk: int = TOPK, max_blocks: int = MAX_BLOCKS, block: int = BLOCK,
+                   replay: int = WINDOW) -> Workload:
     """Requests r = 0.. each with an extend of ``extends[r]`` tokens over
     ``prefixes[r]`` cached tokens (m = 1: one compressed entry per token).  The
     query rows are each request's bounded-replay tail: the last
-    min(128, extend) rows at their absolute positions.  Layers: an L20-style
+    min(replay, extend) rows at their absolute positions (replay = R, 128 in
+    the fixed build; other budgets are the R sweep of "SGLang 如何让 DeepSeek
+    V4.1 Flash 的后半层只处理尾部 token" sec. 3.5, with the SWA width kept at 128).  Layers: an L20-style
     source pass over those rows (normal window, full-visible scoring, top-K and
     candidate pool), an L21-style Reindex layer (pool-restricted scoring, tail
     window) and an L22-style Reuse layer (tail window, the Reindex layer's
     indices)."""
     n_req = len(extends)
     seqs = [p + e for p, e in zip(prefixes, extends)]
-    tails = [min(WINDOW, e) for e in extends]
+    tails = [min(replay, e) for e in extends]
     q_req, q_pos, win = [], [], []
     for r in range(n_req):
         q_req += [r] * tails[r]
@@ -319,7 +323,7 @@ def decoder_replay(extends: List[int], prefixes: List[int], n_heads: int, n_idx_
     L22 = make_layer("L22", "reuse", nq, n_heads, n_idx_heads, late, win, seed, tag, device, False)
     return Workload(tag, 1, n_heads, n_idx_heads, _i32(q_req, device), _i64(q_pos, device), pool,
                     {"L20": L20, "L21": L21, "L22": L22}, topk=topk, block=block,
-                    max_blocks=max_blocks, extend_len=_i32(extends, device),
+                    max_blocks=max_blocks, replay=replay, extend_len=_i32(extends, device),
                     seq_len=_i64(seqs, device), ld=max(seqs))
 
 

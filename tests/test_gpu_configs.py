@@ -186,7 +186,7 @@ def test_c2_decoder_replay(seed):
     run.decoder_tail_step()
     torch.cuda.synchronize()
     assert int(run.d_err.item()) == 0
-    tail, terr = O.tail_layout(npy(w.extend_len), npy(w.seq_len), w.window)
+    tail, terr = O.tail_layout(npy(w.extend_len), npy(w.seq_len), w.replay)
     n = int(tail["cu_tail"][-1])
     assert terr == 0 and n == w.num_q
     for k in ("pos", "win_lo", "src_row", "row_req"):
