@@ -27,6 +27,9 @@
 //   warp 8      TMEM allocation; lane 0 issues the MMAs
 //   warps 9-15  producers: key gather + E2M1 -> f16 into a 4-stage ring, one
 //               key tile of loads in flight ahead of the ring
+// Prologue: the query operand's loads are issued first, the tile geometry is
+// worked out while they are in flight, and the producers start on the key
+// tiles while warps 0-8 dequantise the query operand and allocate TMEM.
 // Waits are time-bounded (CSA2_DERR_TIMEOUT on expiry).
 #include "common.cuh"
 #include "kernels.cuh"
@@ -79,6 +82,8 @@ struct Misc {
   RunInfo runs[kMaxQT];
   int64_t row_len[kMaxQT];   // per query of the tile (0 past the batch)
   int64_t n_vis[kMaxQT];
+  int req[kMaxQT];           // request of each query of the tile
+  int64_t kv0[kMaxQT];       // pool row of that request's entry 0
   int nb[kMaxQT];            // pool mode: candidate blocks per query
   int ident[kMaxQT];         // pool mode: blocks are 0..nb-1
   int cand_smem;             // pool mode: the chunk's candidate blocks are in shared memory
@@ -369,19 +374,20 @@ __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
         const float f = __uint_as_float(x);
         return f + fabsf(f);
       };
-      // four partial sums (heads h mod 4): independent FMA chains
+      // four partial sums (heads h mod 4): independent FMA chains, two per
+      // packed FP32x2 FMA
       auto dot = [&](int ql, int h0, const uint32_t *v, int n, float acc) {
         const float4 *w4 = reinterpret_cast<const float4 *>(ms->w + ql * HI + h0);
-        float a0 = acc, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        float2 a01 = make_float2(acc, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int h = 0; h < n; h += 4) {
           const float4 wv = w4[h / 4];
-          a0 = fmaf(wv.x, relu2(v[h]), a0);
-          a1 = fmaf(wv.y, relu2(v[h + 1]), a1);
-          a2 = fmaf(wv.z, relu2(v[h + 2]), a2);
-          a3 = fmaf(wv.w, relu2(v[h + 3]), a3);
+          a01 = __ffma2_rn(make_float2(wv.x, wv.y), make_float2(relu2(v[h]), relu2(v[h + 1])),
+                           a01);
+          a23 = __ffma2_rn(make_float2(wv.z, wv.w),
+                           make_float2(relu2(v[h + 2]), relu2(v[h + 3])), a23);
         }
-        return (a0 + a1) + (a2 + a3);
+        return (a01.x + a01.y) + (a23.x + a23.y);
       };
       if constexpr (HI == 32) {
         // two queries' columns in flight per TMEM wait
@@ -432,6 +438,29 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
   const int y = blockIdx.y;
   const int warp = threadIdx.x >> 5;
   int err = 0;
+  // ---- query operand loads first: they depend on nothing below, so they are
+  // in flight while the tile geometry is worked out (rows past the tile read
+  // query row 0 and are zeroed).  The epilogue and MMA warps build B; the
+  // producer warps start on the key tiles as soon as the geometry is known.
+  constexpr int kSetupThreads = kProdWarp0 * 32;
+  constexpr int kBItems = (kBRows * 4 + kSetupThreads - 1) / kSetupThreads;
+  uint4 bc[kBItems];
+  float bsc[kBItems];
+  uint32_t bvalid = 0;
+  if (warp < kProdWarp0) {
+#pragma unroll
+    for (int k = 0; k < kBItems; ++k) {
+      const int i = threadIdx.x + k * kSetupThreads;
+      const int row = (i >> 2) % kBRows, grp = i & 3;
+      const int ql = row / HI, h = row % HI;
+      const int q = q0 + ql;
+      const bool v = i < kBRows * 4 && ql < QT && q < P.b.num_q;
+      bvalid |= (v ? 1u : 0u) << k;
+      const int64_t base = v ? (int64_t)q * HI + h : 0;
+      bc[k] = __ldg(reinterpret_cast<const uint4 *>(P.q_fp4 + base * 64) + grp);
+      bsc[k] = __ldg(P.q_scale + base * 4 + grp);
+    }
+  }
   // ---- tile geometry -------------------------------------------------------
   // per query: visible entries and the row length seen by this key chunk.  In
   // pool mode only the candidate blocks overlapping this chunk's slots are
@@ -490,9 +519,12 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
     const int ql = threadIdx.x, q = q0 + ql;
     if (q < P.b.num_q) {
       const int r = P.b.q_req[q];
-      int64_t nv = n_visible(P.b.q_pos[q], P.b.ratio);
-      if (nv > P.b.kv_len[r]) {
-        nv = P.b.kv_len[r];
+      const int64_t pos = P.b.q_pos[q];
+      const int64_t kvl = P.b.kv_len[r];
+      const int64_t kv0 = P.b.kv_start[r];
+      int64_t nv = n_visible(pos, P.b.ratio);
+      if (nv > kvl) {
+        nv = kvl;
         if (y == 0) err |= CSA2_DERR_RANGE_CTX;
       }
       int64_t len = nv;
@@ -510,15 +542,18 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
       ms->row_len[ql] = len;
       ms->n_vis[ql] = nv;
       ms->ident[ql] = ident;
+      ms->req[ql] = r;
+      ms->kv0[ql] = kv0;
     }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
+    // runs: consecutive queries of one request share key tiles (shared memory only)
     int nr = 0;
     for (int ql = 0; ql < QT; ++ql) {
       const int q = q0 + ql;
       if (q >= P.b.num_q) break;
-      const int r = P.b.q_req[q];
+      const int r = ms->req[ql];
       const int gather = P.cand && !ms->ident[ql];
       const int64_t len = ms->row_len[ql];
       const int64_t lim = len < ms->n_vis[ql] ? len : ms->n_vis[ql];
@@ -528,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
         if (len > ru.len) ru.len = len;
         if (lim > ru.lim) ru.lim = lim;
       } else {
-        ms->runs[nr].kv0 = P.b.kv_start[r];
+        ms->runs[nr].kv0 = ms->kv0[ql];
         ms->runs[nr].ql0 = ql;
         ms->runs[nr].nq = 1;
         ms->runs[nr].req = r;
@@ -549,55 +584,41 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
     raise_err(P.d_err, err);
     return;
   }
-  // ---- query operand B: (query, head) rows x 128 f16, and head weights ----
-  uint8_t *B = smem + kOffB;
-  constexpr int kBItems = (kBRows * 4 + kThreads - 1) / kThreads;
-  {
-    // all loads first (rows past the tile read query row 0 and are zeroed)
-    uint4 c[kBItems];
-    float sc[kBItems];
-    uint32_t valid = 0;
+  if (warp < kProdWarp0) {
+    // ---- query operand B: (query, head) rows x 128 f16, and head weights ----
+    uint8_t *B = smem + kOffB;
 #pragma unroll
     for (int k = 0; k < kBItems; ++k) {
-      const int i = threadIdx.x + k * kThreads;
-      const int row = (i >> 2) % kBRows, grp = i & 3;
-      const int ql = row / HI, h = row % HI;
-      const int q = q0 + ql;
-      const bool v = i < kBRows * 4 && ql < QT && q < P.b.num_q;
-      valid |= (v ? 1u : 0u) << k;
-      const int64_t base = v ? (int64_t)q * HI + h : 0;
-      c[k] = __ldg(reinterpret_cast<const uint4 *>(P.q_fp4 + base * 64) + grp);
-      sc[k] = __ldg(P.q_scale + base * 4 + grp);
-    }
-#pragma unroll
-    for (int k = 0; k < kBItems; ++k) {
-      const int i = threadIdx.x + k * kThreads;
+      const int i = threadIdx.x + k * kSetupThreads;
       if (i < kBRows * 4) {
         const int row = i >> 2, grp = i & 3;
         uint4 o[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
                       make_uint4(0, 0, 0, 0)};
-        if ((valid >> k) & 1u) {
-          if (!mx_scale_ok(sc[k]) && y == 0) err |= CSA2_DERR_SCALE;
-          dequant32(c[k], sc[k], o);
+        if ((bvalid >> k) & 1u) {
+          if (!mx_scale_ok(bsc[k]) && y == 0) err |= CSA2_DERR_SCALE;
+          dequant32(bc[k], bsc[k], o);
         }
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
           *reinterpret_cast<uint4 *>(B + sw128_offset(row, grp * 32 + cc * 8, kBBlock)) = o[cc];
       }
     }
+    for (int i = threadIdx.x; i < QT * HI; i += kSetupThreads) {
+      const int q = q0 + i / HI;
+      ms->w[i] = (q < P.b.num_q) ? 0.5f * (P.head_w ? P.head_w[(int64_t)q * HI + i % HI] : 1.f)
+                                 : 0.f;
+    }
+    fence_proxy_async_smem();
+    if (warp == kMmaWarp) {
+      tmem_alloc(&ms->tmem_base, 512);
+      tmem_relinquish();
+    }
+    // the epilogue and MMA warps wait for B, the weights and the TMEM base;
+    // the producers are already on their way
+    fence_before_sync();
+    asm volatile("bar.sync 1, %0;" ::"n"(kSetupThreads) : "memory");
+    fence_after_sync();
   }
-  for (int i = threadIdx.x; i < QT * HI; i += kThreads) {
-    const int q = q0 + i / HI;
-    ms->w[i] = (q < P.b.num_q) ? 0.5f * (P.head_w ? P.head_w[(int64_t)q * HI + i % HI] : 1.f) : 0.f;
-  }
-  fence_proxy_async_smem();
-  if (warp == kMmaWarp) {
-    tmem_alloc(&ms->tmem_base, 512);
-    tmem_relinquish();
-  }
-  fence_before_sync();
-  __syncthreads();
-  fence_after_sync();
   if (warp < kEpiWarps) {
     epilogue_role<HI>(P, smem, ms, q0, y);
   } else if (warp == kMmaWarp) {
