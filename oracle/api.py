@@ -39,9 +39,12 @@ def lib():
         for name in ("oracle_tail_layout", "oracle_index_score", "oracle_topk",
                      "oracle_topk_candidates", "oracle_sparse_swa_attn",
                      "oracle_sparse_swa_attn_fp4kv", "oracle_encoder_replay_layout",
-                     "oracle_rows_gather", "oracle_rows_scatter"):
+                     "oracle_rows_gather", "oracle_rows_scatter", "oracle_encode_rows",
+                     "oracle_encode_e4m3", "oracle_encode_e2m1"):
             getattr(_lib, name).restype = C.c_int
         _lib.oracle_decode_fp4kv_row.restype = None
+        _lib.oracle_encode_e4m3.argtypes = [C.c_double]
+        _lib.oracle_encode_e2m1.argtypes = [C.c_double]
     return _lib
 
 
@@ -156,6 +159,30 @@ def rows_scatter(row_idx, src, dst):
     err = lib().oracle_rows_scatter(C.c_int64(idx.shape[0]), _p(idx), _p(s), _p(d),
                                     C.c_int64(d.shape[0]), C.c_int64(rb))
     return d, err
+
+
+FMT_FP8_B32, FMT_FP4KV, FMT_MXFP4 = 1, 2, 3
+
+
+def encode_e4m3(x: float) -> int:
+    return int(lib().oracle_encode_e4m3(float(x)))
+
+
+def encode_e2m1(x: float) -> int:
+    return int(lib().oracle_encode_e2m1(float(x)))
+
+
+def encode_rows(fmt, src, dst_row, codes, scales):
+    """Quantise rows of src (fp32 [n, dim]) into rows dst_row of (codes,
+    scales) in place of copies; returns (codes, scales, err)."""
+    x = _c(src, np.float32)
+    n, dim = x.shape
+    dr = _c(dst_row, np.int64)
+    cd = np.array(codes, copy=True, order="C")
+    sc = np.array(scales, copy=True, order="C")
+    err = lib().oracle_encode_rows(C.c_int(fmt), C.c_int64(n), _p(x), C.c_int(dim), _p(dr),
+                                   _p(cd), _p(sc), C.c_int64(cd.shape[0]))
+    return cd, sc, err
 
 
 def index_score(b, q_fp4, q_scale, head_w, k_fp4, k_scale, ld,

@@ -44,6 +44,13 @@
  *                    the late layers is cut to the tail rows, and the computed
  *                    tail rows are scattered back into the full extend layout
  *                    (the other rows are left as they were).
+ *   cache writes     mixed-precision card (main KV FP8 block-32 or E2M1 with an
+ *                    E4M3 scale per 16, index K MXFP4 per 32) and article sec.
+ *                    5 ("保持量化语义的融合": a fused quantise-and-write keeps
+ *                    the rounding sequence of the unfused one).  Reading: the
+ *                    group scale is computed in fp32, x / scale in fp32, and
+ *                    the element rounds to nearest (ties to even) with
+ *                    saturation at the format's largest finite value.
  *   attention        article sec. 1: each query attends to its own 128-token
  *                    window and to at most 512 selected compressed positions;
  *                    one softmax over both sets; the 512-dim latent row is both
@@ -66,7 +73,8 @@ enum {
   OR_ERR_LD = 16,
   OR_ERR_CAPACITY = 32,
   OR_ERR_BAD_EXTEND = 64,
-  OR_ERR_RANGE_ROW = 256
+  OR_ERR_RANGE_ROW = 256,
+  OR_ERR_NONFINITE = 512
 };
 
 typedef struct {
@@ -119,6 +127,103 @@ static double fp4kv_elem(const uint8_t *codes, const uint8_t *sf, int d) {
   int byte = codes[d / 2];
   int nib = (d & 1) ? (byte >> 4) : (byte & 15);
   return oracle_e2m1_value(nib) * oracle_e4m3_value(sf[d / 16]);
+}
+
+/* Round x to the nearest code of a sign-magnitude format whose non-negative
+ * codes 0..max_code have increasing values val(c): the nearest magnitude by
+ * brute force, a tie going to the code with an even last bit; magnitudes
+ * beyond val(max_code) saturate to it.  The sign bit is copied from x (a
+ * negative value that rounds to zero keeps its sign), as IEEE rounding does. */
+static int encode_nearest(double x, int max_code, int sign_shift, double (*val)(int)) {
+  const int neg = signbit(x) ? 1 : 0;
+  const double a = fabs(x);
+  int best = max_code;
+  if (a < val(max_code)) {
+    double bd = INFINITY;
+    for (int c = 0; c <= max_code; ++c) {
+      const double d = fabs(val(c) - a);
+      if (d < bd || (d == bd && (c & 1) == 0)) {
+        bd = d;
+        best = c;
+      }
+    }
+  }
+  return best | (neg << sign_shift);
+}
+
+int oracle_encode_e4m3(double x) { return encode_nearest(x, 126, 7, oracle_e4m3_value); }
+int oracle_encode_e2m1(double x) { return encode_nearest(x, 7, 3, oracle_e2m1_value); }
+
+/* Quantise-and-write of cache rows.  Row i of src (dim fp32 values) goes to
+ * row dst_row[i] of the destination (skipped when negative; past `rows` it is
+ * skipped and RANGE_ROW is set).  A group holding a NaN or an infinity is
+ * written as zero codes with the neutral scale and sets NONFINITE.
+ *   format 1, FP8 block-32: s = amax / 448 (fp32; 1 when that is 0), codes
+ *     E4M3(x / s); codes [rows, dim], scales fp32 [rows, dim/32].
+ *   format 2, FP4 main KV: sc = E4M3(amax / 6), s = value(sc), codes
+ *     E2M1(x / s) (0 when s is 0); codes [rows, dim/2], sf [rows, dim/16].
+ *   format 3, MXFP4: s = 2^(floor(log2 amax) - 2) (1 when amax is 0), codes
+ *     E2M1(x / s); codes [rows, dim/2], scales fp32 [rows, dim/32]; a scale
+ *     outside [2^-23, 2^12] sets SCALE (0 as a scale: written as a zero group).
+ * Element 2i of an E2M1 row sits in the low nibble of byte i. */
+int oracle_encode_rows(int format, int64_t n, const float *src, int dim, const int64_t *dst_row,
+                       uint8_t *codes, void *scales, int64_t rows) {
+  int err = 0;
+  const int gs = format == 2 ? 16 : 32;
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t r = dst_row[i];
+    if (r < 0) continue;
+    if (r >= rows) {
+      err |= OR_ERR_RANGE_ROW;
+      continue;
+    }
+    const float *x = src + i * dim;
+    for (int g = 0; g < dim / gs; ++g) {
+      float amax = 0.0f;
+      int bad = 0;
+      for (int e = 0; e < gs; ++e) {
+        const float v = x[g * gs + e];
+        if (!isfinite(v)) bad = 1;
+        else if (fabsf(v) > amax) amax = fabsf(v);
+      }
+      float s = 1.0f;
+      int zero = bad;
+      uint8_t sf = 0;
+      if (bad) {
+        err |= OR_ERR_NONFINITE;
+      } else if (format == 1) {
+        s = amax / 448.0f;
+        if (s == 0.0f) s = 1.0f;
+      } else if (format == 2) {
+        sf = (uint8_t)oracle_encode_e4m3((double)(amax / 6.0f));
+        s = (float)oracle_e4m3_value(sf);
+        if (s == 0.0f) zero = 1;
+      } else if (amax > 0.0f) {
+        int ex = 0;
+        (void)frexpf(amax, &ex);
+        s = ldexpf(1.0f, ex - 3);
+        if (s == 0.0f || s < 0x1p-23f || s > 0x1p12f) err |= OR_ERR_SCALE;
+        if (s == 0.0f) {
+          s = 1.0f;
+          zero = 1;
+        }
+      }
+      for (int e = 0; e < gs; ++e) {
+        const int d = g * gs + e;
+        const float q = zero ? 0.0f : x[d] / s;
+        if (format == 1) {
+          codes[r * dim + d] = (uint8_t)oracle_encode_e4m3((double)q);
+        } else {
+          const int c = oracle_encode_e2m1((double)q);
+          uint8_t *b = codes + r * (dim / 2) + d / 2;
+          *b = (d & 1) ? (uint8_t)((*b & 0x0f) | (c << 4)) : (uint8_t)((*b & 0xf0) | c);
+        }
+      }
+      if (format == 2) ((uint8_t *)scales)[r * (dim / 16) + g] = bad ? 0 : sf;
+      else ((float *)scales)[r * (dim / 32) + g] = s;
+    }
+  }
+  return err;
 }
 
 /* One FP4 main-KV row of `dim` elements decoded to double (used by the pins). */
