@@ -46,6 +46,8 @@ def parse():
                     help="skip the FP4 main-KV attention measurement")
     ap.add_argument("--no-rows", action="store_true",
                     help="skip the tail cut / scatter-back measurement")
+    ap.add_argument("--no-quant", action="store_true",
+                    help="skip the cache quantise-and-write measurement")
     ap.add_argument("--no-cpu", action="store_true")
     return ap.parse_args()
 
@@ -228,6 +230,7 @@ def bench_ours(args, rank, world, local_rank):
 
     fp4 = None if args.no_fp4kv else bench_fp4kv(args, w, run, stream, flush, hbm)
     cut = None if args.no_rows else bench_rows(args, w, run, stream, flush, hbm)
+    quant = None if args.no_quant else bench_quant(args, w, stream, flush, hbm)
 
     e2e = None
     if not args.no_e2e:
@@ -235,7 +238,7 @@ def bench_ours(args, rank, world, local_rank):
 
     return dict(value=value, ms=ms, wall=wall, clocks=clk, roofline=roofline, e2e=e2e,
                 launches=launches_per_step * args.steps, rows=rows, w=w, fp4kv=fp4,
-                rows_copy=cut)
+                rows_copy=cut, quant=quant)
 
 
 def bench_fp4kv(args, w, run, stream, flush, hbm):
@@ -319,6 +322,49 @@ def bench_rows(args, w, run, stream, flush, hbm):
     return {"kernel": "csa2_rows_gather / csa2_rows_scatter",
             "rows": f"{run.nq} tail rows of {n_full}, {row_bytes} B each (mHC state)",
             "peak_gbs": hbm, **res}
+
+
+def bench_quant(args, w, stream, flush, hbm):
+    """Quantise-and-write of the entries the L20-style source pass of the step
+    completes: 8 x 8192 main-KV entries (fp32 latent rows of 512 -> FP8
+    block-32, and -> the FP4 main-KV layout) and their index keys (fp32 rows of
+    128 -> MXFP4).  Timed per launch with events, L2 flushed between launches."""
+    import torch
+    import sparse_attention_prefill_gb300 as S
+    dev = w.q_pos.device
+    n = int(w.extend_len.sum().item())
+    g = torch.Generator(device=dev).manual_seed(args.seed + 17)
+    d_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    dst = torch.arange(n, dtype=torch.int64, device=dev)
+    cases = []
+    for name, fmt, dim, cshape, sshape, sdt in (
+            ("main_kv_fp8_b32", S.FMT_FP8_B32, 512, (n, 512), (n, 16), torch.float32),
+            ("main_kv_fp4", S.FMT_FP4KV, 512, (n, 256), (n, 32), torch.uint8),
+            ("index_k_mxfp4", S.FMT_MXFP4, 128, (n, 64), (n, 4), torch.float32)):
+        src = torch.randn((n, dim), generator=g, device=dev, dtype=torch.float32)
+        codes = torch.empty(cshape, dtype=torch.uint8, device=dev)
+        scales = torch.empty(sshape, dtype=sdt, device=dev)
+        fn = lambda: S.quantize_rows(fmt, src, dst, codes, scales, d_err)   # noqa: E731
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(max(5, min(args.steps, 20))):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in ts) / len(ts)
+        byts = n * (dim * 4 + 8 + codes.shape[1] + scales.shape[1] * scales.element_size())
+        cases.append({"case": name, "rows": n, "avg_launch_ms": round(ms, 4),
+                      "algorithmic_bytes_per_launch": int(byts),
+                      "achieved_gbs": round(byts / (ms * 1e-3) / 1e9, 1),
+                      "frac": round(byts / (ms * 1e-3) / 1e9 / hbm, 4)})
+        del src, codes, scales
+    assert int(d_err.item()) == 0
+    return {"kernel": "csa2_quantize_rows", "peak_gbs": hbm, "cases": cases}
 
 
 def run_kernel_id():
@@ -546,7 +592,7 @@ def main():
                 "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r["e2e"],
                 "clocks": r["clocks"], "gpu_launches": r["launches"],
                 "wall_s_timed_region": round(r["wall"], 4), "fp4_kv_attention": r["fp4kv"],
-                "tail_cut_restore": r["rows_copy"]}
+                "tail_cut_restore": r["rows_copy"], "cache_write": r["quant"]}
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

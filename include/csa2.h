@@ -73,6 +73,12 @@ typedef struct CUstream_st *csa2_stream_t; /* same object as cudaStream_t */
 #define CSA2_DERR_BAD_EXTEND 64   /* an extend with E < 0 or S < E */
 #define CSA2_DERR_TIMEOUT 128     /* a pipeline wait inside a kernel gave up (internal error) */
 #define CSA2_DERR_RANGE_ROW 256   /* a row index past the rows of a gather source / scatter target */
+#define CSA2_DERR_NONFINITE 512   /* a NaN or infinity in a group being quantised */
+
+/* storage formats of csa2_quantize_rows */
+#define CSA2_FMT_FP8_B32 1        /* E4M3 codes + fp32 scale per 32 */
+#define CSA2_FMT_FP4KV 2          /* E2M1 codes + E4M3 scale per 16 */
+#define CSA2_FMT_MXFP4 3          /* E2M1 codes + power-of-two fp32 scale per 32 */
 
 /* Rows of one layer call.  Host struct; every array is device memory.
  *   q_req[Nq]   request of each query row (0 <= q_req < num_req)
@@ -317,6 +323,41 @@ CSA2_API int csa2_rows_scatter(const int32_t *count, int64_t capacity,
                          const int32_t *row_idx, const void *src, void *dst,
                          int64_t dst_rows, int64_t row_bytes, int32_t *d_err,
                          csa2_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Quantise-and-write of cache rows   [CSA2] mixed-precision card (main KV FP8
+ * block-32 or "E2M1 数据；每 16 通道一个 E4M3 scale", index K MXFP4 per 32);
+ * [D0] sec. 5 ("保持量化语义的融合": fusing the quantise, pack and cache write
+ * must keep the intermediate rounding and scaling).
+ *
+ * Row i of src ([n, dim] fp32, 16-byte aligned) is quantised into row
+ * dst_row[i] of a cache of `rows` rows.  Per group of G channels with
+ * amax = max |x|:
+ *   CSA2_FMT_FP8_B32 (G = 32): s = amax / 448 in fp32 (1 if that is 0);
+ *       codes [rows, dim] E4M3(x / s); scales fp32 [rows, dim/32] = s.
+ *   CSA2_FMT_FP4KV   (G = 16): sc = E4M3(amax / 6), s = value(sc);
+ *       codes [rows, dim/2] E2M1(x / s) (0 if s is 0); scales uint8
+ *       [rows, dim/16] = sc.
+ *   CSA2_FMT_MXFP4   (G = 32): s = 2^(floor(log2 amax) - 2) (1 if amax is 0);
+ *       codes [rows, dim/2] E2M1(x / s); scales fp32 [rows, dim/32] = s.  A
+ *       scale outside [2^-23, 2^12] sets CSA2_DERR_SCALE (the readers'
+ *       range); one that underflows to 0 writes the group as zeros, scale 1.
+ * x / s is an fp32 division; E4M3 / E2M1 round to nearest, ties to even,
+ * saturating at 448 / 6 (a negative value rounding to zero keeps its sign).
+ * E2M1 element 2i sits in the low nibble of byte i.  A group holding a NaN or
+ * infinity is written as zero codes with scale 1 (FP4KV: scale code 0) and
+ * sets CSA2_DERR_NONFINITE.  dst_row[i] < 0 skips row i; dst_row[i] >= rows
+ * skips it and sets CSA2_DERR_RANGE_ROW.  Destination rows are expected to
+ * be distinct.  dim % G == 0, dim <= 16384; codes 16-byte aligned (FP8) or
+ * 8-byte aligned (E2M1).
+ * The encoder-replay write protocol uses it with the layout of
+ * csa2_encoder_replay_layout: SWA rows for every processed row, global
+ * entries only for [entry_range[2r], entry_range[2r+1]); cached entries are
+ * never named, hence never rewritten.
+ * ------------------------------------------------------------------------- */
+CSA2_API int csa2_quantize_rows(int32_t format, int64_t n, const float *src, int32_t dim,
+                         const int64_t *dst_row, uint8_t *codes, void *scales,
+                         int64_t rows, int32_t *d_err, csa2_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -23,11 +23,13 @@ LIB_PATH = os.path.join(_HERE, "_build", "libcsa2.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 DERR_RANGE_IDX, DERR_RANGE_WINDOW, DERR_RANGE_CTX = 1, 2, 4
 DERR_SCALE, DERR_LD, DERR_CAPACITY, DERR_BAD_EXTEND = 8, 16, 32, 64
-DERR_TIMEOUT, DERR_RANGE_ROW = 128, 256
+DERR_TIMEOUT, DERR_RANGE_ROW, DERR_NONFINITE = 128, 256, 512
+FMT_FP8_B32, FMT_FP4KV, FMT_MXFP4 = 1, 2, 3
 
 EXPORTED = ("csa2_status_string", "csa2_tail_layout", "csa2_index_score", "csa2_topk",
             "csa2_topk_candidates", "csa2_sparse_swa_attn", "csa2_sparse_swa_attn_fp4kv",
-            "csa2_encoder_replay_layout", "csa2_rows_gather", "csa2_rows_scatter")
+            "csa2_encoder_replay_layout", "csa2_rows_gather", "csa2_rows_scatter",
+            "csa2_quantize_rows")
 
 
 class Csa2Error(RuntimeError):
@@ -70,6 +72,7 @@ def load(path: Optional[str] = None):
                                                i64, vp, vp]
     lib.csa2_rows_gather.argtypes = [vp, i64, vp, vp, i64, vp, i64, vp, vp]
     lib.csa2_rows_scatter.argtypes = [vp, i64, vp, vp, vp, i64, i64, vp, vp]
+    lib.csa2_quantize_rows.argtypes = [i32, i64, vp, i32, vp, vp, vp, i64, vp, vp]
     for name in EXPORTED[1:]:
         getattr(lib, name).restype = C.c_int
     _lib = lib
@@ -196,6 +199,13 @@ def csa2_rows_scatter(count, capacity, row_idx, src, dst, dst_rows, row_bytes, d
                                     _stream(stream))
 
 
+def csa2_quantize_rows(fmt, n, src, dim, dst_row, codes, scales, rows, d_err,
+                       stream=None) -> int:
+    return load().csa2_quantize_rows(int(fmt), int(n), _ptr(src), int(dim), _ptr(dst_row),
+                                     _ptr(codes), _ptr(scales), int(rows), _ptr(d_err),
+                                     _stream(stream))
+
+
 # allocating conveniences (torch allocates the outputs; the library computes)
 # ---------------------------------------------------------------------------
 
@@ -254,6 +264,15 @@ def rows_scatter(row_idx, src, dst, count=None, d_err=None, stream=None):
     _check(csa2_rows_scatter(count, int(row_idx.shape[0]), row_idx, src, dst, int(dst.shape[0]),
                              rb, d_err, stream), "csa2_rows_scatter")
     return dst
+
+
+def quantize_rows(fmt, src, dst_row, codes, scales, d_err=None, stream=None):
+    """Quantise fp32 rows src [n, dim] into rows dst_row of a cache
+    (codes, scales) in one of the FMT_* layouts; returns (codes, scales)."""
+    n, dim = int(src.shape[0]), int(src.shape[1])
+    _check(csa2_quantize_rows(fmt, n, src, dim, dst_row, codes, scales, int(codes.shape[0]),
+                              d_err, stream), "csa2_quantize_rows")
+    return codes, scales
 
 
 def index_score(batch, q_fp4, q_scale, head_w, k_fp4, k_scale, ld, cand_blocks=None, block=8,
