@@ -413,19 +413,33 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms) {
     const bool meta_ok = wait_bar(&ms->meta_full[ms_slot], (qi >> 1) & 1, ms);
     asm volatile("cp.async.wait_all;" ::: "memory");
     if (!meta_ok) break;
-    for (int it = ptid; it < P.n_heads * (kDim / 8); it += kProducerThreads) {
-      const int h = it / (kDim / 8), d = (it % (kDim / 8)) * 8;
-      uint4 *p4 = reinterpret_cast<uint4 *>(Qs + sw128_offset(h, d, kQBlock));
-      const uint4 raw = *p4;
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-      uint32_t o[4];
+    // in batches: every shared-memory read of a batch is issued before its
+    // conversions and stores
+    constexpr int kQBatch = 3;
+    const int q_chunks = P.n_heads * (kDim / 8);
+    for (int base = ptid; base < q_chunks; base += kQBatch * kProducerThreads) {
+      uint4 raw[kQBatch];
+      uint32_t off[kQBatch];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xffff0000u);
-        __half2 hh = __floats2half2_rn(lo, hi);
-        o[j] = *reinterpret_cast<uint32_t *>(&hh);
+      for (int k = 0; k < kQBatch; ++k) {
+        const int it = base + k * kProducerThreads;
+        const int h = it / (kDim / 8), d = (it % (kDim / 8)) * 8;
+        off[k] = sw128_offset(h, d, kQBlock);
+        if (it < q_chunks) raw[k] = *reinterpret_cast<const uint4 *>(Qs + off[k]);
       }
-      *p4 = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+      for (int k = 0; k < kQBatch; ++k) {
+        if (base + k * kProducerThreads >= q_chunks) break;
+        const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xffff0000u);
+          __half2 hh = __floats2half2_rn(lo, hi);
+          o[j] = *reinterpret_cast<uint32_t *>(&hh);
+        }
+        *reinterpret_cast<uint4 *>(Qs + off[k]) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
     }
     fence_proxy_async_smem();
     __syncwarp();
@@ -600,6 +614,24 @@ __device__ void o_issuer_role(const Params &P, uint8_t *smem, Misc *ms) {
 // ---------------------------------------------------------------------------
 // softmax + epilogue (warps 0-7)
 // ---------------------------------------------------------------------------
+// Reduce 32 per-lane values across the warp so that lane j ends with the
+// reduction of value j over all lanes: five halving steps, each lane keeping
+// the half of the values whose index bit matches its lane bit.  v is consumed.
+template <class Op>
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane, Op op) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = upper ? v[i] : v[i + o];
+      const float keep = upper ? v[i + o] : v[i];
+      v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, o));
+    }
+  }
+  return v[0];
+}
+
 __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sp = warp & 3;          // TMEM sub-partition: lanes 32*sp ..
@@ -674,14 +706,10 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
       if (slow) {
         // per-head maximum over the warp's rows (butterfly per head), then
         // across the 4 warps of this head half
-        float mine = NEG_INF;
+        float xm[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          float mj = x[j];
-#pragma unroll
-          for (int w = 16; w >= 1; w >>= 1) mj = fmaxf(mj, __shfl_xor_sync(0xffffffffu, mj, w));
-          if (lane == j) mine = mj;
-        }
+        for (int j = 0; j < 32; ++j) xm[j] = x[j];
+        const float mine = reduce_scatter32(xm, lane, [](float a, float b) { return fmaxf(a, b); });
         ms->red[sp][32 * hh + lane] = mine;
         if (!(ok = group_sync(&ms->sm_grp, gp, ms))) break;
         if (stid < 64) {
@@ -744,14 +772,8 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
     }
     if (!ok) break;
     // ---- epilogue: row sums, normalisation, bf16 output, lse
-    float lmine = 0.f;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      float lj = lsum[j];
-#pragma unroll
-      for (int w = 16; w >= 1; w >>= 1) lj += __shfl_xor_sync(0xffffffffu, lj, w);
-      if (lane == j) lmine = lj;
-    }
+    // lane j: the warp's sum of lsum[j] (recursive halving: 31 shuffles)
+    const float lmine = reduce_scatter32(lsum, lane, [](float a, float b) { return a + b; });
     ms->red[sp][32 * hh + lane] = lmine;
     if (!(ok = group_sync(&ms->sm_grp, gp, ms))) break;
     if (stid < 64) {
