@@ -36,6 +36,8 @@
 //               issued one step ahead
 // Every wait is bounded (about two seconds); on expiry the kernel raises
 // CSA2_DERR_TIMEOUT, drains and returns.
+#include <cuda.h>   // CUtensorMap (the encoder is reached through the runtime)
+
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tcgen05.cuh"
@@ -81,7 +83,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kDerrTimeout = 128;
 
 struct Misc {
-  uint64_t q_full, q_empty, o_full, o_empty, done, done_o, sm_grp;
+  uint64_t q_full, q_empty, q_tma, o_full, o_empty, done, done_o, sm_grp;
   uint64_t r_full[2], r_empty[2][2], s_full[2], s_empty[2], p_full[2], p_empty[2];
   uint64_t meta_full[2];
   int64_t meta[2][4];   // per query (ring of 2): selected rows, window rows, first SWA
@@ -372,7 +374,8 @@ __device__ __forceinline__ void store_step(uint8_t *R, int half, bool swap, int 
 }
 
 template <bool kFp4>
-__device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms) {
+__device__ void producer_role(const Params &P, const CUtensorMap *tmap_q, uint8_t *smem,
+                              Misc *ms) {
   const int ptid = threadIdx.x - kProducerWarp0 * 32;
   const int lane = threadIdx.x & 31;
   const int row0 = ptid >> 5, seg = lane;
@@ -391,28 +394,21 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms) {
   uint32_t g = 0;  // chunks produced by this CTA
   uint32_t qi = 0;
   for (int q = blockIdx.x; q < P.b.num_q; q += gridDim.x, ++qi) {
-    // ---- Q of this query (f16, heads zero-padded to 64)
+    // ---- Q of this query: eight 64 x 64 bf16 boxes by TMA, landing in the
+    // SW128 layout (heads past n_heads are the map's zero fill); converted to
+    // f16 in place below (f16 and bf16 are both 2 bytes)
     if (!wait_bar(&ms->q_empty, (qi & 1) ^ 1, ms)) break;
-    const __nv_bfloat16 *qg = P.q + (int64_t)q * P.n_heads * kDim;
-    // raw bf16 chunks land at their final swizzled place; each thread then
-    // converts exactly the chunks it copied (f16 and bf16 are both 2 bytes)
-    for (int it = ptid; it < kHeadsPad * (kDim / 8); it += kProducerThreads) {
-      const int h = it / (kDim / 8), d = (it % (kDim / 8)) * 8;
-      uint8_t *dst = Qs + sw128_offset(h, d, kQBlock);
-      if (h < P.n_heads) {
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
-                     "l"(qg + (int64_t)h * kDim + d)
-                     : "memory");
-      } else {
-        *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
-      }
+    if (ptid == 0) {
+      mbar_arrive_expect_tx(&ms->q_tma, kHeadsPad * kDim * 2);
+#pragma unroll
+      for (int b = 0; b < kDim / 64; ++b)
+        tma_load_3d(Qs + b * kQBlock, tmap_q, b * 64, 0, q, &ms->q_tma);
     }
     // ---- row list and counts of this query (built one query ahead by the
     // first softmax warp)
     const uint32_t ms_slot = qi & 1;
-    const bool meta_ok = wait_bar(&ms->meta_full[ms_slot], (qi >> 1) & 1, ms);
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    if (!meta_ok) break;
+    if (!wait_bar(&ms->meta_full[ms_slot], (qi >> 1) & 1, ms)) break;
+    if (!wait_bar(&ms->q_tma, qi & 1, ms)) break;
     // in batches: every shared-memory read of a batch is issued before its
     // conversions and stores
     constexpr int kQBatch = 3;
@@ -815,13 +811,15 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
 }
 
 template <bool kFp4>
-__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(Params P) {
+__global__ void __launch_bounds__(kThreads, 1)
+attn_tc_kernel(Params P, const __grid_constant__ CUtensorMap tmap_q) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Misc *ms = reinterpret_cast<Misc *>(smem + kOffMisc);
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     mbar_init(&ms->q_full, kProducerWarps);
     mbar_init(&ms->q_empty, 1);
+    mbar_init(&ms->q_tma, 1);
     mbar_init(&ms->o_full, 1);
     mbar_init(&ms->o_empty, kSoftmaxWarps);
     mbar_init(&ms->done, 1);
@@ -854,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(Params P) {
   } else if (warp == kOWarp) {
     o_issuer_role(P, smem, ms);
   } else {
-    producer_role<kFp4>(P, smem, ms);
+    producer_role<kFp4>(P, &tmap_q, smem, ms);
   }
   fence_before_sync();
   __syncthreads();
@@ -863,6 +861,44 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(Params P) {
     fence_after_sync();
     tmem_dealloc(ms->tmem_base, kTmemCols);
   }
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library)
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_tiled() {
+  static EncodeTiled fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult res;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &res) == cudaSuccess &&
+        res == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  }
+  return fn;
+}
+
+// Q [num_q, n_heads, 512] bf16 as a 3-D map (dims, heads, queries) with
+// 64 x 64 x 1 boxes in 128-byte swizzle: one box is one 64-channel block of
+// the SW128 operand tile; heads past n_heads read as zeros.
+bool make_q_map(CUtensorMap *map, const __nv_bfloat16 *q, int n_heads, int num_q) {
+  EncodeTiled fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)kDim, (cuuint64_t)n_heads, (cuuint64_t)num_q};
+  const cuuint64_t strides[2] = {(cuuint64_t)kDim * 2, (cuuint64_t)n_heads * kDim * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kHeadsPad, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16 *>(q), dims,
+            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int sm_count() {
@@ -911,14 +947,16 @@ int attn_tc(const Batch &b, int n_heads, const __nv_bfloat16 *q, const uint8_t *
   P.lse = lse;
   P.d_err = d_err;
   const int grid = b.num_q < sm_count() ? b.num_q : sm_count();
+  CUtensorMap tmap_q;
+  if (!make_q_map(&tmap_q, q, n_heads, b.num_q)) return CSA2_ERR_UNSUPPORTED;
   if (kv_sf) {
     cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)kSmemBytes);
-    attn_tc_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(P);
+    attn_tc_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(P, tmap_q);
   } else {
     cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)kSmemBytes);
-    attn_tc_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(P);
+    attn_tc_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(P, tmap_q);
   }
   return launch_status();
 }

@@ -227,6 +227,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Arrive on `bar` and announce `bytes` of asynchronous copies that complete
+// on it (the phase completes once the arrivals and the bytes are all in).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.release.cta.shared::cta.b64 st, [%0], "
+      "%1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+// TMA: one box of a 3-D tensor map into shared memory, completing on `bar`.
+// The innermost coordinate x must be a multiple of 16 bytes' worth of
+// elements; the destination is 1024-byte aligned for 128-byte swizzling.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, int y, int z,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Wait for the phase with the given parity to complete.  Gives up after
 // `limit` polls (each try_wait itself blocks for a bounded hardware interval)
 // and returns false so the caller can raise an error instead of hanging.
