@@ -408,10 +408,37 @@ __device__ void producer_role(const Params &P, const CUtensorMap *tmap_q, uint8_
     // first softmax warp)
     const uint32_t ms_slot = qi & 1;
     if (!wait_bar(&ms->meta_full[ms_slot], (qi >> 1) & 1, ms)) break;
+    const int *list = lists + ms_slot * kMaxSel;
+    Src S;
+    S.nsel = ms->meta[ms_slot][0];
+    S.nrows = S.nsel + ms->meta[ms_slot][1];
+    const int64_t win_first = ms->meta[ms_slot][2];
+    const int64_t kv0 = ms->meta[ms_slot][3];
+    if (kFp4) {
+      S.sel_b = P.kv_fp8 + kv0 * (kDim / 2) + seg * 8;
+      S.sel_sf = P.kv_sf + kv0 * (kDim / 16) + seg;
+      S.sel_s = nullptr;
+    } else {
+      S.sel_b = P.kv_fp8 + kv0 * kDim + seg * 16;
+      S.sel_s = P.kv_scale + kv0 * (kDim / 32) + seg / 2;
+      S.sel_sf = nullptr;
+    }
+    S.win_b = P.swa_fp8 + win_first * kDim + seg * 16;
+    S.win_s = P.swa_scale + win_first * (kDim / 32) + seg / 2;
+    S.dummy_b = P.swa_fp8 + seg * 16;
+    S.dummy_s = P.swa_scale + seg / 2;
+    const int nch = n_chunks_of(S.nrows);
+    // ---- chunks: 2 steps of 32 rows each; the loads of the next step are
+    // in flight while a step waits for its buffer and is stored
+    const int nsteps = nch * 2;
+    Item b0[kItemsPerThread], b1[kItemsPerThread];
+    // the first step's rows are loaded before Q is converted: their latency
+    // overlaps the copy and the conversion
+    load_step<kFp4>(list, S, row0, 0, b0);
     if (!wait_bar(&ms->q_tma, qi & 1, ms)) break;
     // in batches: every shared-memory read of a batch is issued before its
     // conversions and stores
-    constexpr int kQBatch = 3;
+    constexpr int kQBatch = 4;
     const int q_chunks = P.n_heads * (kDim / 8);
     for (int base = ptid; base < q_chunks; base += kQBatch * kProducerThreads) {
       uint4 raw[kQBatch];
@@ -440,31 +467,6 @@ __device__ void producer_role(const Params &P, const CUtensorMap *tmap_q, uint8_
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&ms->q_full);
-    const int *list = lists + ms_slot * kMaxSel;
-    Src S;
-    S.nsel = ms->meta[ms_slot][0];
-    S.nrows = S.nsel + ms->meta[ms_slot][1];
-    const int64_t win_first = ms->meta[ms_slot][2];
-    const int64_t kv0 = ms->meta[ms_slot][3];
-    if (kFp4) {
-      S.sel_b = P.kv_fp8 + kv0 * (kDim / 2) + seg * 8;
-      S.sel_sf = P.kv_sf + kv0 * (kDim / 16) + seg;
-      S.sel_s = nullptr;
-    } else {
-      S.sel_b = P.kv_fp8 + kv0 * kDim + seg * 16;
-      S.sel_s = P.kv_scale + kv0 * (kDim / 32) + seg / 2;
-      S.sel_sf = nullptr;
-    }
-    S.win_b = P.swa_fp8 + win_first * kDim + seg * 16;
-    S.win_s = P.swa_scale + win_first * (kDim / 32) + seg / 2;
-    S.dummy_b = P.swa_fp8 + seg * 16;
-    S.dummy_s = P.swa_scale + seg / 2;
-    const int nch = n_chunks_of(S.nrows);
-    // ---- chunks: 2 steps of 32 rows each; the loads of the next step are
-    // in flight while a step waits for its buffer and is stored
-    const int nsteps = nch * 2;
-    Item b0[kItemsPerThread], b1[kItemsPerThread];
-    load_step<kFp4>(list, S, row0, 0, b0);
     bool ok = true;
     // one step: prefetch step st+1 into `pre`, then store step st from `use`
     auto step = [&](int st, Item(&use)[kItemsPerThread], Item(&pre)[kItemsPerThread]) -> bool {
