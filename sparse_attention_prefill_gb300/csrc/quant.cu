@@ -8,8 +8,9 @@
 // E4M3(amax / 6); 2^(floor(log2 amax) - 2)), x / scale in fp32, then the
 // hardware round-to-nearest-even conversion with saturation (cvt.rn.satfinite).
 //
-// One warp per source row, 16 consecutive channels per lane and pass (a
-// 32-channel group is a lane pair); rows go to dst_row[i] of the cache, so
+// One warp per source row (rows narrower than 512 channels share a warp), 16
+// consecutive channels per lane and pass (a 32-channel group is a lane pair);
+// rows go to dst_row[i] of the cache, so
 // one launch writes the entries a step completes wherever they live.  HBM
 // bound: 4 B read and 1.125 / 0.5625 B written per channel.
 #include "common.cuh"
@@ -58,22 +59,26 @@ quantize_rows_kernel(int64_t n, const float *__restrict__ src, int dim,
                      void *__restrict__ scales, int64_t rows, int32_t *__restrict__ d_err) {
   constexpr int kGroup = kFmt == CSA2_FMT_FP4KV ? 16 : 32;
   const int lane = threadIdx.x & 31;
-  const int chunks = dim / 16;
-  const int passes = (chunks + 31) / 32;
+  const int chunks = dim / 16;   // 16-channel chunks per row
+  // narrow rows (a power-of-two count of chunks below 32) share a warp
+  const int rpw = (chunks < 32 && (32 % chunks) == 0) ? 32 / chunks : 1;
+  const int lpr = rpw > 1 ? chunks : 32;   // lanes per row
+  const int sub = lane / lpr, cl = lane % lpr;
+  const int passes = rpw > 1 ? 1 : (chunks + 31) / 32;
   int err = 0;
-  for (int64_t i = (int64_t)blockIdx.x * kQWarps + (threadIdx.x >> 5); i < n;
-       i += (int64_t)gridDim.x * kQWarps) {
-    const int64_t r = dst_row[i];   // the same for the whole warp
-    if (r < 0) continue;
-    if (r >= rows) {
-      err |= CSA2_DERR_RANGE_ROW;
-      continue;
-    }
+  for (int64_t base = ((int64_t)blockIdx.x * kQWarps + (threadIdx.x >> 5)) * rpw; base < n;
+       base += (int64_t)gridDim.x * kQWarps * rpw) {
+    const int64_t i = base + sub;
+    const bool row_ok = i < n;
+    const int64_t r = row_ok ? dst_row[i] : -1;
+    const bool write = r >= 0 && r < rows;
+    if (row_ok && r >= rows) err |= CSA2_DERR_RANGE_ROW;
     for (int p = 0; p < passes; ++p) {
-      const int c = lane + 32 * p;   // chunk of 16 channels
-      const bool has = c < chunks;
+      const int c = cl + 32 * p;   // chunk of 16 channels
+      const bool has = write && c < chunks;
       float v[16];
-      const float4 *s4 = reinterpret_cast<const float4 *>(src + i * dim + 16 * (has ? c : 0));
+      const float4 *s4 =
+          reinterpret_cast<const float4 *>(src + (row_ok ? i : 0) * dim + 16 * (c < chunks ? c : 0));
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const float4 f = __ldcs(s4 + k);
@@ -171,7 +176,9 @@ extern "C" CSA2_API int csa2_quantize_rows(int32_t format, int64_t n, const floa
   if (((uintptr_t)src & 15u) || ((uintptr_t)codes & (format == CSA2_FMT_FP8_B32 ? 15u : 7u)) ||
       ((uintptr_t)scales & 3u))
     return CSA2_ERR_UNSUPPORTED;
-  const int64_t want = (n + csa2::kQWarps - 1) / csa2::kQWarps;
+  const int chunks = dim / 16;
+  const int64_t rpw = (chunks < 32 && (32 % chunks) == 0) ? 32 / chunks : 1;
+  const int64_t want = (n + csa2::kQWarps * rpw - 1) / (csa2::kQWarps * rpw);
   const int64_t cap = (int64_t)csa2::sm_count() * (2048 / csa2::kQThreads);
   const int grid = (int)(want < cap ? want : cap);
   cudaStream_t st = csa2::as_stream(stream);

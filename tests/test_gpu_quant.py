@@ -43,7 +43,8 @@ def _run(fmt, x, dst, rows, fill=0x5A):
 
 @pytest.mark.parametrize("fmt,dim", [(S.FMT_FP8_B32, 512), (S.FMT_FP4KV, 512),
                                      (S.FMT_MXFP4, 128), (S.FMT_FP8_B32, 96),
-                                     (S.FMT_FP4KV, 1040), (S.FMT_MXFP4, 1536)])
+                                     (S.FMT_FP4KV, 1040), (S.FMT_MXFP4, 1536),
+                                     (S.FMT_MXFP4, 64), (S.FMT_FP8_B32, 32), (S.FMT_FP4KV, 16)])
 def test_quantize_rows_bit_exact(fmt, dim):
     rng = np.random.default_rng(fmt * 1000 + dim)
     n = 300
