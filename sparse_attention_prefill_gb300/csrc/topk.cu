@@ -10,11 +10,12 @@
 // an ineligible element); the selection is exactly the k largest keys, ties
 // by lowest position, which is the pinned total order's top k.
 //  - Rows of up to 16384 keys are held in registers (256 threads, KPT keys
-//    each, loaded together).  The k-th key of a strided sample, at a rank
-//    scaled to the sample plus a margin, bounds the threshold from below;
-//    the keys above it (typically ~1.5k) are compacted into shared memory and
-//    an 8-bit radix search finds the exact k-th key on that list alone.  A
-//    missed estimate falls back to the same search over the whole row.
+//    each, loaded together).  A threshold guess from the mean and deviation
+//    of a strided sample (the score a normal row of those moments would have
+//    ~2k + 64 scores above) picks the keys that are compacted into shared
+//    memory (typically ~1.1k); an 8-bit radix search finds the exact k-th key
+//    on that list alone.  A guess that lists fewer than k keys or more than
+//    the list holds falls back to the same search over the whole row.
 //  - Longer rows: a 4-pass radix select over the row staged in shared memory
 //    (or re-read from L2), then keys > T emitted directly and the keys equal
 //    to T taken in position order by a block-wide ordered scan.
@@ -204,7 +205,7 @@ __device__ uint32_t select_topk(const Keys &keys, int64_t n, uint32_t k, SelectS
 }
 
 constexpr int kListCap = 4096;      // compacted candidates of one row (2x the largest k)
-constexpr int kSampleSlots = 4;      // register slots per thread in the threshold sample
+constexpr int kSampleSlots = 4;      // register slots per thread in the moment sample
 
 template <int NT>
 struct RegShared {
@@ -293,12 +294,11 @@ __device__ void radix_kth(Each each, uint32_t mn, uint32_t mx, uint32_t k, RegSh
 // Selection for a row held in registers: thread t owns positions t + j*NT
 // (key[j], 0 = ineligible; slots j >= jn hold no keys).
 //  1. Count the eligible keys; if at most k, all are selected.
-//  2. Rows of more than 2*kSampleSlots keys per thread: find the k-th key of a
-//     strided sample (kSampleSlots slots per thread), at a rank scaled to the
-//     sample with a margin, and compact every key >= that estimate into a
+//  2. Guess a threshold from the moments of a strided sample (kSampleSlots
+//     slots per thread) and compact every key >= the guess into a
 //     shared-memory list.  With between k and kListCap keys listed, the exact
-//     search runs on the list alone; otherwise (a rare miss of the estimate)
-//     on the whole row.
+//     search runs on the list alone; otherwise (a missed guess) on the whole
+//     row.  Any guess is safe: only the cost depends on it.
 //  3. Emit the keys >= lo; keys equal to the threshold, if only some of them
 //     are taken, go in position order by a block scan over the row.
 template <int NT, int KPT, class Emit>
@@ -306,7 +306,8 @@ __device__ uint32_t select_topk_regs(const uint32_t (&key)[KPT], int jn, uint32_
                                      RegShared<NT> &sh, Emit emit) {
   constexpr int kStride = KPT / kSampleSlots > 0 ? KPT / kSampleSlots : 1;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  uint32_t cnt = 0, mx = 0, s_cnt = 0, s_mn = 0xffffffffu, s_mx = 0;
+  uint32_t cnt = 0, mx = 0, f_cnt = 0;
+  float f_sum = 0.f, f_sq = 0.f;   // moments of a strided sample of the finite scores
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {
     if (j >= jn) break;
@@ -314,38 +315,43 @@ __device__ uint32_t select_topk_regs(const uint32_t (&key)[KPT], int jn, uint32_
     cnt += x != 0u;
     mx = max(mx, x);
     if (j % kStride == 0) {
-      s_cnt += x != 0u;
-      s_mn = min(s_mn, x ? x : 0xffffffffu);
-      s_mx = max(s_mx, x);
+      const float f = __uint_as_float((x & 0x80000000u) ? x ^ 0x80000000u : ~x);
+      const bool fin = x != 0u && fabsf(f) <= 3.0e38f;
+      f_cnt += fin;
+      f_sum += fin ? f : 0.f;
+      f_sq += fin ? f * f : 0.f;
     }
   }
   cnt = __reduce_add_sync(0xffffffffu, cnt);
   mx = __reduce_max_sync(0xffffffffu, mx);
-  s_cnt = __reduce_add_sync(0xffffffffu, s_cnt);
-  s_mn = __reduce_min_sync(0xffffffffu, s_mn);
-  s_mx = __reduce_max_sync(0xffffffffu, s_mx);
+  f_cnt = __reduce_add_sync(0xffffffffu, f_cnt);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    f_sum += __shfl_xor_sync(0xffffffffu, f_sum, o);
+    f_sq += __shfl_xor_sync(0xffffffffu, f_sq, o);
+  }
   if (lane == 0) {
     sh.red[0][warp] = cnt;
     sh.red[2][warp] = mx;
-    sh.red[3][warp] = s_cnt;
-    sh.red[4][warp] = s_mn;
-    sh.red[5][warp] = s_mx;
+    sh.red[3][warp] = f_cnt;
+    sh.red[4][warp] = __float_as_uint(f_sum);
+    sh.red[5][warp] = __float_as_uint(f_sq);
   }
   for (int i = t; i < 256; i += NT) sh.hist[i] = 0;
   if (t == 0) sh.out_count = 0;
   __syncthreads();
   uint32_t n_elig = 0;
-  cnt = 0;
   mx = 0;
-  s_mn = 0xffffffffu;
-  s_mx = 0;
+  f_cnt = 0;
+  f_sum = 0.f;
+  f_sq = 0.f;
 #pragma unroll
   for (int w = 0; w < NT / 32; ++w) {
     n_elig += sh.red[0][w];
     mx = max(mx, sh.red[2][w]);
-    cnt += sh.red[3][w];
-    s_mn = min(s_mn, sh.red[4][w]);
-    s_mx = max(s_mx, sh.red[5][w]);
+    f_cnt += sh.red[3][w];
+    f_sum += __uint_as_float(sh.red[4][w]);
+    f_sq += __uint_as_float(sh.red[5][w]);
   }
   if (n_elig <= k) {  // everything eligible is selected
 #pragma unroll
@@ -362,20 +368,21 @@ __device__ uint32_t select_topk_regs(const uint32_t (&key)[KPT], int jn, uint32_
   bool whole;
   bool listed = false;
   uint32_t n_list = 0;
-  if (jn > 2 * kSampleSlots && cnt > 0) {
-    // sample rank matching rank k of the row, plus a margin (~3 sigma)
-    const uint64_t r0 = ((uint64_t)k * cnt * 13) / (10ull * n_elig) + 16;
-    const uint32_t rs = (uint32_t)(r0 < cnt ? r0 : cnt);
-    radix_kth<NT>(
-        [&](auto f) {
-#pragma unroll
-          for (int j = 0; j < KPT; j += kStride)
-            if (j < jn) f(key[j]);
-        },
-        s_mn, s_mx, rs, sh, prefix, rem, whole);
-    // the sample's rs-th key (an eligible key, so t_est >= 1): keys >= t_est
-    // are counted, offsets taken by a block scan, and written if they fit
-    const uint32_t t_est = prefix;
+  // first guess: the score expected to have about 2k + 64 scores above it if
+  // the row were normal with its own mean and deviation (the same value in
+  // every thread; any guess is safe, a bad one only falls through to the
+  // sample estimate)
+  uint32_t t_est = 0;
+  if (f_cnt > 1) {
+    const float mean = f_sum / (float)f_cnt;
+    const float sd = sqrtf(fmaxf(f_sq / (float)f_cnt - mean * mean, 0.f));
+    const float p = (float)(2u * k + 64u) / (float)n_elig;
+    if (p < 1.f && sd > 0.f) t_est = score_key(mean + 1.41421356f * erfcinvf(2.f * p) * sd);
+  }
+  if (t_est != 0u) {
+    // keys >= t_est are counted and offset by a block scan, and written to
+    // the list if at least k and at most its capacity are: the list then
+    // holds the whole selection
     uint32_t mine = 0;
 #pragma unroll
     for (int j = 0; j < KPT; ++j) {
@@ -394,7 +401,6 @@ __device__ uint32_t select_topk_regs(const uint32_t (&key)[KPT], int jn, uint32_
         }
       }
       __syncthreads();
-      // every key of the selection is >= t_est, hence listed
       listed = true;
       radix_kth<NT>(
           [&](auto f) {

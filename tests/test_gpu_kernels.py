@@ -173,10 +173,10 @@ def test_topk_full_mode_bit_exact(n, k):
 def test_topk_special_rows_bit_exact(n, k):
     """Rows of every register-path size with degenerate contents: all keys
     equal, ties straddling the k-th key, fewer than k eligible entries, one
-    eligible entry, dense coarse-grid scores, and -0/+0 (equal scores, so
-    entry order decides) at the k-th key."""
+    eligible entry, dense coarse-grid scores, -0/+0 (equal scores, so entry
+    order decides) at the k-th key, and rows that defeat the threshold guess."""
     rng = np.random.default_rng(7 * n + k)
-    q_pos = [n - 1] * 7 + [k - 1, n // 3, n - 1]
+    q_pos = [n - 1] * 7 + [k - 1, n // 3, n - 1, n - 1, n - 1]
     s = (np.round(rng.standard_normal((len(q_pos), n)) * 4) / 4).astype(np.float32)
     s[0, :] = 1.5                                         # all equal
     s[1, :] = np.where(rng.random(n) < 0.5, 2.0, -1.0)    # two values
@@ -189,6 +189,13 @@ def test_topk_special_rows_bit_exact(n, k):
     s[6, :] = np.float32(1e-40)                           # subnormal, all equal
     s[9, :] = np.where(rng.random(n) < 0.5, np.float32(-0.0), np.float32(0.0))
     s[9, rng.choice(n, k // 2, replace=False)] = 1.0      # -0 and +0 tie at the k-th key
+    # rows whose moments mislead a normal-quantile threshold guess: a few far
+    # outliers inflate the deviation (too few keys listed), or a tight cluster
+    # sits just above a long left tail (too many)
+    s[10, :] = (rng.standard_normal(n) * 0.01).astype(np.float32)
+    s[10, rng.choice(n, max(1, n // 64), replace=False)] = 100.0
+    s[11, :] = (5.0 + rng.standard_normal(n) * 1e-3).astype(np.float32)
+    s[11, rng.choice(n, max(1, n // 5), replace=False)] = -1000.0
     b = _sel_batch(q_pos, n)
     ref_idx, ref_cnt, _ = O.topk(np_batch(b), s, k)
     idx, cnt = S.topk(_to(b), torch.from_numpy(s).to(DEV), k)
