@@ -903,19 +903,6 @@ bool make_q_map(CUtensorMap *map, const __nv_bfloat16 *q, int n_heads, int num_q
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int sm_count() {
-  static int cached[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  if (!cached[dev]) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = n > 0 ? n : 1;
-  }
-  return cached[dev];
-}
-
 }  // namespace
 
 int attn_tc(const Batch &b, int n_heads, const __nv_bfloat16 *q, const uint8_t *kv_codes,

@@ -22,6 +22,20 @@ static inline int launch_status() {
   return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
 }
 
+// SM count of the current device (cached per device); grids are sized by it.
+static inline int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
+}
+
 // ---------------------------------------------------------------------------
 // batch view on the device (plain copy of the host struct's pointers)
 // ---------------------------------------------------------------------------

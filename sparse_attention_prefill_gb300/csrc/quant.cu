@@ -146,19 +146,6 @@ quantize_rows_kernel(int64_t n, const float *__restrict__ src, int dim,
   if (lane == 0) raise_err(d_err, err);
 }
 
-int sm_count() {
-  static int cached[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  if (!cached[dev]) {
-    int c = 0;
-    cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = c > 0 ? c : 1;
-  }
-  return cached[dev];
-}
-
 }  // namespace
 }  // namespace csa2
 

@@ -65,19 +65,6 @@ rows_copy_kernel(const int32_t *__restrict__ count, int64_t capacity,
   if (lane == 0) raise_err(d_err, err);
 }
 
-int sm_count() {
-  static int cached[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  if (!cached[dev]) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = n > 0 ? n : 1;
-  }
-  return cached[dev];
-}
-
 template <bool kScatter>
 int rows_copy(const int32_t *count, int64_t capacity, const int32_t *row_idx, const void *src,
               void *dst, int64_t other_rows, int64_t row_bytes, int32_t *d_err,
