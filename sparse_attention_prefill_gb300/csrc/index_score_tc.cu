@@ -41,7 +41,7 @@ namespace {
 using namespace tc;
 
 constexpr int kKeyTile = 128;
-constexpr int kTilesPerChunk = 16;
+constexpr int kTilesPerChunk = 32;
 constexpr int kStages = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kMmaWarp = 8;
