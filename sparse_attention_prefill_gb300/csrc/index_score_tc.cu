@@ -17,7 +17,7 @@
 // per-head dots are exact; only the fp32 head sum rounds.
 //
 // Work unit (one CTA): a tile of 256/Hi consecutive query rows and a chunk of
-// 16 key tiles (2048 keys or pool slots).  Rows of the tile that belong to the
+// 32 key tiles (4096 keys or pool slots).  Rows of the tile that belong to the
 // same request share key tiles ("runs", full mode); in pool mode every query
 // has its own slot list and is its own run, except that identity pools
 // (blocks 0, 1, ..., nb-1: nothing excluded, the case when every reachable
