@@ -17,9 +17,9 @@
 // the K-major A operand of the first product and the MN-major A operand of
 // the second.  Chunks are double-buffered in shared memory (R and P), S^T in
 // TMEM (2 x 64 columns; an M = 64 accumulator fills lanes 0-15 of each 32-lane
-// sub-partition) and O^T takes 4 x 64 TMEM columns.  The MMA issuer runs S^T
-// one chunk ahead of O^T, so gathering, softmax and both products of
-// neighbouring chunks overlap.  The softmax keeps a lazily moved reference
+// sub-partition) and O^T takes 4 x 64 TMEM columns.  S^T runs one chunk ahead
+// of O^T (each has its own issuing warp), so gathering, softmax and both
+// products of neighbouring chunks overlap.  The softmax keeps a lazily moved reference
 // maximum per head: it moves (and O^T and the row sums are rescaled) only when
 // a logit exceeds it by more than 2^8, so P <= 256 always fits f16.
 //
@@ -31,9 +31,12 @@
 //   warp 9      lane 0 issues the O^T MMAs (the two products of neighbouring
 //               chunks are issued independently, so neither waits behind the
 //               other in one issuing thread)
-//   warps 10-15 producers: Q (bf16 -> f16 via cp.async, converted in place),
-//               row gather + E4M3 -> f16 dequant in steps of 32 rows, loads
-//               issued one step ahead
+//   warps 10-15 producers: Q by TMA (eight 64 x 64 boxes of a 3-D tensor map
+//               in 128-byte swizzle, converted bf16 -> f16 in place), row
+//               gather + E4M3 -> f16 dequant in steps of 32 rows, loads issued
+//               one step ahead; a chunk buffer is released in 32-row halves
+// The per-query row sums and maxima are reduced across a warp's lanes with a
+// reduce-scatter (five halving steps).
 // Every wait is bounded (about two seconds); on expiry the kernel raises
 // CSA2_DERR_TIMEOUT, drains and returns.
 #include <cuda.h>   // CUtensorMap (the encoder is reached through the runtime)
