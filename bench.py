@@ -519,9 +519,17 @@ def cpu_baseline(w, budget_s=15.0):
         n += oracle_sample_step(w, rows_per_req, threads)
         reps += 1
     dt = time.perf_counter() - t0
+    # the same oracle on one thread, one tail row per request
+    t1 = time.perf_counter()
+    n1 = oracle_sample_step(w, 1, 1)
+    dt1 = time.perf_counter() - t1
+    from oracle import api as O
+    O.set_threads(threads)
     return {"value": len(LAYERS) * n / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": "%d x (%d tail rows per request x 8 requests) through the 3-layer step"
-                      % (reps, rows_per_req)}
+                      % (reps, rows_per_req),
+            "single_thread": {"value": len(LAYERS) * n1 / dt1, "cores": 1,
+                              "sample": "1 tail row per request x 8 requests through the 3-layer step"}}
 
 
 def config_block(w, extra=None):
