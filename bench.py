@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--no-quant", action="store_true",
                     help="skip the cache quantise-and-write measurement")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--configs", action="store_true",
+                    help="instead of the bench line: layer-queries/s of each of the five workloads")
     return ap.parse_args()
 
 
@@ -367,6 +369,61 @@ def bench_quant(args, w, stream, flush, hbm):
     return {"kernel": "csa2_quantize_rows", "peak_gbs": hbm, "cases": cases}
 
 
+def bench_configs(args):
+    """Layer-queries/s of each named workload's call sequence (the sequences the
+    full-size parity tests run), one JSON line per workload.  Events around each
+    sequence, L2 flushed before each, 2 warm-up and 5 timed repetitions."""
+    import torch
+    from sparse_attention_prefill_gb300 import synth
+    from sparse_attention_prefill_gb300.layer import LayerRunner
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for name in synth.CONFIG_NAMES:
+        w = synth.config(name, dev, args.seed)
+        if name == "c5_ragged_mixed":
+            req = w.q_req.cpu()
+            ri = torch.nonzero(req % 2 == 0).flatten().to(dev)
+            ru = torch.nonzero(req % 2 == 1).flatten().to(dev)
+            run_ri, run_ru = LayerRunner(w, ri), LayerRunner(w, ru)
+            given = w.layers["mixed"].given_idx[ru].contiguous()
+            seq = lambda: (run_ri.reindex_layer("mixed", None),   # noqa: E731
+                           run_ru.reuse_layer("mixed", given))
+            rows, layers = w.num_q, 1
+            d_errs = [run_ri.d_err, run_ru.d_err]
+        else:
+            run = LayerRunner(w)
+            if name == "c2_decoder_replay":
+                seq, layers = run.decoder_tail_step, 3
+            elif name == "c4_hierarchical":
+                seq = lambda: run.reindex_layer("L21", run.source_layer("L20"))   # noqa: E731
+                layers = 2
+            else:
+                seq, layers = (lambda: run.full_layer("full")), 1
+            rows = run.nq
+            d_errs = [run.d_err]
+        for _ in range(2):
+            seq()
+        ts = []
+        for _ in range(5):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            seq()
+            e1.record()
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        assert all(int(d.item()) == 0 for d in d_errs), name
+        ms = sum(a.elapsed_time(b) for a, b in ts) / len(ts)
+        print(json.dumps({"workload": name, "query_rows": rows, "layers": layers,
+                          "ms_per_sequence": round(ms, 4),
+                          "layer_queries_per_s": round(layers * rows / (ms * 1e-3), 1)}),
+              flush=True)
+        del w
+        torch.cuda.empty_cache()
+    return 0
+
+
 def run_kernel_id():
     """Identity of the attention kernel build (source hash) so that stored ncu
     traffic is only reported for the kernel it was measured on."""
@@ -580,6 +637,8 @@ def main():
         print(json.dumps(line))
         return 0
 
+    if args.configs:
+        return bench_configs(args) if rank == 0 else 0
     import torch
     if world > 1:
         torch.distributed.init_process_group("nccl")
