@@ -74,3 +74,21 @@ def test_host_validation_of_replay_and_row_calls():
     fake = ctypes.c_void_p(4096)
     assert lib.csa2_rows_gather(None, i64(4), fake, fake, i64(8), fake, i64(24), None,
                                 None) == 2
+
+
+def test_status_and_flag_values_agree():
+    """The header's status codes, data-error bits and format ids, the binding's
+    constants and the oracle's own copy of the error bits name the same
+    values (the three are written separately)."""
+    import sparse_attention_prefill_gb300 as S
+    src = open(os.path.join(ROOT, "include", "csa2.h")).read()
+    hdr = {m.group(1): int(m.group(2))
+           for m in re.finditer(r"#define CSA2_(\w+)\s+(\d+)", src)}
+    for name, val in hdr.items():
+        if name.startswith(("OK", "ERR_", "DERR_", "FMT_")):
+            assert getattr(S, name) == val, name
+    bits = [v for k, v in hdr.items() if k.startswith("DERR_")]
+    assert len(bits) == len(set(bits)) and all(b & (b - 1) == 0 for b in bits)
+    osrc = open(os.path.join(ROOT, "oracle", "csa2_oracle.c")).read()
+    for m in re.finditer(r"OR_ERR_(\w+) = (\d+)", osrc):
+        assert hdr["DERR_" + m.group(1)] == int(m.group(2)), m.group(1)
