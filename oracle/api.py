@@ -27,7 +27,9 @@ class _Batch(C.Structure):
 def lib():
     global _lib
     if _lib is None:
-        _lib = C.CDLL(build_oracle())
+        # CSA2_ORACLE_LIB points the pins at another build of this file (the
+        # mutation tests load deliberately broken copies through it)
+        _lib = C.CDLL(os.environ.get("CSA2_ORACLE_LIB") or build_oracle())
         _lib.oracle_e2m1_value.restype = C.c_double
         _lib.oracle_e2m1_value.argtypes = [C.c_int]
         _lib.oracle_e4m3_value.restype = C.c_double
