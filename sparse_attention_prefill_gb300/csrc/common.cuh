@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/csa2.h"
 
 namespace csa2 {
@@ -22,18 +24,21 @@ static inline int launch_status() {
   return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
 }
 
-// SM count of the current device (cached per device); grids are sized by it.
+// SM count of the current device (cached per device; concurrent first calls
+// store the same value); grids are sized by it.
 static inline int sm_count() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
-  if (!cached[dev]) {
+  int c = cached[dev].load(std::memory_order_relaxed);
+  if (c == 0) {
     int n = 0;
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = n > 0 ? n : 1;
+    c = n > 0 ? n : 1;
+    cached[dev].store(c, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return c;
 }
 
 // ---------------------------------------------------------------------------
