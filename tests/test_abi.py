@@ -92,3 +92,19 @@ def test_status_and_flag_values_agree():
     osrc = open(os.path.join(ROOT, "oracle", "csa2_oracle.c")).read()
     for m in re.finditer(r"OR_ERR_(\w+) = (\d+)", osrc):
         assert hdr["DERR_" + m.group(1)] == int(m.group(2)), m.group(1)
+
+
+def test_binding_argtypes_match_header_prototypes():
+    """Every entry point's ctypes prototype in the binding has as many
+    arguments as the header declares (catches signature drift)."""
+    import sparse_attention_prefill_gb300 as S
+    from sparse_attention_prefill_gb300 import build
+    src = open(os.path.join(ROOT, "include", "csa2.h")).read()
+    protos = dict(re.findall(r"CSA2_API\s+(?:const\s+char\s*\*|int)\s*(csa2_\w+)\s*\(([^;]*)\)\s*;",
+                             src, re.S))
+    assert set(protos) == set(_declared())
+    lib = S.load(build.build())
+    for name, params in protos.items():
+        n = 0 if params.strip() in ("", "void") else params.count(",") + 1
+        assert len(getattr(lib, name).argtypes) == n, name
+    assert set(S.EXPORTED) == set(protos)
