@@ -368,10 +368,10 @@ __device__ uint32_t select_topk_regs(const uint32_t (&key)[KPT], int jn, uint32_
   bool whole;
   bool listed = false;
   uint32_t n_list = 0;
-  // first guess: the score expected to have about 2k + 64 scores above it if
-  // the row were normal with its own mean and deviation (the same value in
-  // every thread; any guess is safe, a bad one only falls through to the
-  // sample estimate)
+  // threshold guess: the score expected to have about 2k + 64 scores above it
+  // if the row were normal with its sample's mean and deviation (the same
+  // value in every thread; any guess is safe, a bad one only falls through to
+  // the search over the whole row)
   uint32_t t_est = 0;
   if (f_cnt > 1) {
     const float mean = f_sum / (float)f_cnt;
