@@ -321,3 +321,41 @@ def test_host_argument_checks():
     assert S.csa2_topk(_to(b), s, 10, 0, None, 8, 2048, idx, cnt, None) == S.ERR_INVALID_ARG
     bb = dict(_to(b), ratio=3)
     assert S.csa2_topk(bb, s, 10, 4, None, 8, 2048, idx, cnt, None) == S.ERR_INVALID_ARG
+
+
+def test_attention_reference_moves_mid_query():
+    """Window rows 64 times larger than the selected rows: their logits jump
+    far past the reference set by the first chunks, so the softmax moves the
+    per-head reference in a later chunk and rescales the O accumulator and
+    the row sums already gathered."""
+    w, b, L, idx, sk = _attn_case(64, 512, nq=9, ctx=3000, seed=21)
+    swa_scale = (L.swa_scale * 64.0).contiguous()
+    ref_o, ref_l, rerr = O.sparse_swa_attn(np_batch(b), npy(L.q), npy(w.pool.kv_fp8),
+                                           npy(w.pool.kv_scale), npy(idx), npy(L.swa_fp8),
+                                           npy(swa_scale), None, 128, w.sm_scale)
+    d_err = _derr()
+    o, l = S.sparse_swa_attn(_to(b), L.q.to(DEV), w.pool.kv_fp8.to(DEV), w.pool.kv_scale.to(DEV),
+                             idx.to(DEV), L.swa_fp8.to(DEV), swa_scale.to(DEV), None, 128,
+                             w.sm_scale, d_err=d_err)
+    assert int(d_err.item()) == rerr == 0
+    assert_attn_close(o, None, ref_o, None)
+    # lse: its error is at most the largest logit error, and a logit errs by at
+    # most sm_scale * 2^-10 * sum_d |q_d r_d| (f16 rows: the f16 scale and the
+    # f16 product each round once).  The logits here are ~64x the unit-variance
+    # ones, and so is that bound.
+    tab = np.array([O.e4m3_value(c) for c in range(256)])
+    rows_of = lambda codes, sc: tab[codes.astype(np.int64)] * np.repeat(   # noqa: E731
+        sc.astype(np.float64), 32, axis=1)
+    kv = rows_of(npy(w.pool.kv_fp8), npy(w.pool.kv_scale))
+    sw = rows_of(npy(L.swa_fp8), npy(swa_scale))
+    nb = np_batch(b)
+    q = L.q.float().numpy().astype(np.float64)
+    bound = np.zeros(ref_l.shape)
+    for i in range(ref_l.shape[0]):
+        t, r = int(nb["q_pos"][i]), int(nb["q_req"][i])
+        rows = [kv[int(nb["kv_start"][r]) + int(j)] for j in npy(idx)[i] if j >= 0]
+        rows += [sw[int(nb["swa_start"][r]) + p - int(nb["swa_pos0"][r])]
+                 for p in range(max(0, t - 127), t + 1)]
+        bound[i] = w.sm_scale * 2.0 ** -10 * (np.abs(q[i]) @ np.abs(np.stack(rows)).T).max(1)
+    d = np.abs(npy(l).astype(np.float64) - ref_l)
+    assert (d <= bound + 1e-5 * np.abs(ref_l)).all(), (d.max(), bound.min())
