@@ -103,10 +103,13 @@ def test_index_score_full_mode(ratio, hi):
     assert int(d_err.item()) == rerr
 
 
-def test_index_score_pool_mode_and_ctx_flag():
+@pytest.mark.parametrize("hi", [32, 16, 8])
+def test_index_score_pool_mode_and_ctx_flag(hi):
+    # hi = 32 keeps a CTA's candidate blocks in shared memory; 16 and 8 (more
+    # queries per tile) read them from global memory
     ctx = 5000
     qpos = [4999, 4000, 17, 2048, 2049]
-    w = synth.full_layer(ctx, 1, qpos, 16, 32, seed=5, tag="ipool")
+    w = synth.full_layer(ctx, 1, qpos, 16, hi, seed=5, tag="ipool%d" % hi)
     b = w.batch("full")
     L = w.layers["full"]
     g = torch.Generator().manual_seed(3)
