@@ -45,6 +45,7 @@ def lib():
                      "oracle_encode_e4m3", "oracle_encode_e2m1"):
             getattr(_lib, name).restype = C.c_int
         _lib.oracle_decode_fp4kv_row.restype = None
+        _lib.oracle_decode_mxfp4_row.restype = None
         _lib.oracle_encode_e4m3.argtypes = [C.c_double]
         _lib.oracle_encode_e2m1.argtypes = [C.c_double]
     return _lib
@@ -281,6 +282,15 @@ def sparse_swa_attn_fp4kv(b, q_bf16, kv_fp4, kv_sf, idx, swa_fp8, swa_scale, win
                                              _p(ss), _p(wl), C.c_int(window),
                                              C.c_double(sm_scale), _p(sk), _p(out), _p(lse))
     return out, lse, err
+
+
+def decode_mxfp4_row(codes, scales):
+    """One MXFP4 row decoded to float64 (codes uint8 [D/2], scales f32 [D/32])."""
+    c, f = _c(codes, np.uint8), _c(scales, np.float32)
+    dim = c.shape[-1] * 2
+    out = np.zeros(dim, np.float64)
+    lib().oracle_decode_mxfp4_row(_p(c), _p(f), C.c_int(dim), _p(out))
+    return out
 
 
 def decode_fp4kv_row(codes, sf):

@@ -226,6 +226,13 @@ int oracle_encode_rows(int format, int64_t n, const float *src, int dim, const i
   return err;
 }
 
+/* One MXFP4 row of `dim` elements decoded to double (used by the pins: the
+ * index score's dot products cannot see the nibble order, which both operands
+ * share, but the rows a quantiser writes must decode in this order). */
+void oracle_decode_mxfp4_row(const uint8_t *codes, const float *scales, int dim, double *out) {
+  for (int d = 0; d < dim; ++d) out[d] = mxfp4_elem(codes, scales, d);
+}
+
 /* One FP4 main-KV row of `dim` elements decoded to double (used by the pins). */
 void oracle_decode_fp4kv_row(const uint8_t *codes, const uint8_t *sf, int dim,
                              double *out) {

@@ -132,3 +132,25 @@ def test_pool_slots_map_to_entries():
             else:
                 assert pool[q, slot] == -np.inf
         assert np.isnan(pool[q, nb * 8:]).all()
+
+
+def test_mxfp4_row_decode_order_and_scales():
+    """Element 2i in the low nibble of byte i, one scale per 32 elements (the
+    layout a quantiser writes; dot products alone cannot see the nibble order)."""
+    codes = np.zeros(64, np.uint8)
+    codes[0] = 0x21        # element 0 = 0.5 (code 1), element 1 = 1.0 (code 2)
+    codes[17] = 0xF7       # element 34 = 6.0 (code 7), element 35 = -6.0 (code 15)
+    scales = np.array([2.0, 0.25, 1.0, 1.0], np.float32)
+    row = O.decode_mxfp4_row(codes, scales)
+    expect = np.zeros(128)
+    expect[0], expect[1] = 1.0, 2.0
+    expect[34], expect[35] = 1.5, -1.5
+    assert (row == expect).all()
+    # round trip through the oracle's own quantiser
+    x = np.linspace(-3, 3, 128).astype(np.float32)[None, :]
+    c, s, err = O.encode_rows(O.FMT_MXFP4, x, np.array([0]), np.zeros((1, 64), np.uint8),
+                              np.zeros((1, 4), np.float32))
+    assert err == 0
+    y = O.decode_mxfp4_row(c[0], s[0])
+    # E2M1's widest gap is 2 units (between 4 and 6): at most 1 unit x scale off
+    assert np.abs(y - x[0]).max() <= s.max()

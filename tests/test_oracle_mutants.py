@@ -47,6 +47,26 @@ MUTANTS = [
      ["test_oracle_quant.py"]),
     ("mxfp4_scale_exponent", "s = ldexpf(1.0f, ex - 3);", "s = ldexpf(1.0f, ex - 2);",
      ["test_oracle_quant.py"]),
+    ("mxfp4_nibble_order",
+     "int nib = (d & 1) ? (byte >> 4) : (byte & 15);\n  return oracle_e2m1_value(nib) * (double)scales",
+     "int nib = (d & 1) ? (byte & 15) : (byte >> 4);\n  return oracle_e2m1_value(nib) * (double)scales",
+     ["test_oracle_index.py"]),
+    ("fp4kv_nibble_order",
+     "int nib = (d & 1) ? (byte >> 4) : (byte & 15);\n  return oracle_e2m1_value(nib) * oracle_e4m3_value",
+     "int nib = (d & 1) ? (byte & 15) : (byte >> 4);\n  return oracle_e2m1_value(nib) * oracle_e4m3_value",
+     ["test_oracle_fp4kv.py"]),
+    ("fp4kv_scale_group", "oracle_e4m3_value(sf[d / 16]);", "oracle_e4m3_value(sf[d / 32]);",
+     ["test_oracle_fp4kv.py"]),
+    ("tail_source_row", "src_row[row] = (int32_t)(cu_e + e - t + k);",
+     "src_row[row] = (int32_t)(cu_e + e - t + k + 1);", ["test_oracle_tail.py"]),
+    ("replay_source_row", "src_row[row] = k < rp ? -1 : (int32_t)(cu_e + (k - rp));",
+     "src_row[row] = k < rp ? -1 : (int32_t)(cu_e + (k - rp) + 1);", ["test_oracle_replay.py"]),
+    ("pool_slot_offset", "j = blk * block + s % block;", "j = blk * block + (s + 1) % block;",
+     ["test_oracle_index.py"]),
+    ("head_weight_dropped", "acc += w * (dot > 0.0 ? dot : 0.0);", "acc += (dot > 0.0 ? dot : 0.0);",
+     ["test_oracle_index.py"]),
+    ("block_tie_order_reversed", "return (x->b > y->b) - (x->b < y->b);",
+     "return (x->b < y->b) - (x->b > y->b);", ["test_oracle_select.py"]),
 ]
 
 
