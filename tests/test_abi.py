@@ -108,3 +108,18 @@ def test_binding_argtypes_match_header_prototypes():
         n = 0 if params.strip() in ("", "void") else params.count(",") + 1
         assert len(getattr(lib, name).argtypes) == n, name
     assert set(S.EXPORTED) == set(protos)
+
+
+def test_missing_library_fails_loudly():
+    """No CPU fallback: without libcsa2.so the binding raises instead of computing."""
+    import subprocess
+    import sys
+    code = ("import sparse_attention_prefill_gb300 as S\n"
+            "try:\n"
+            "    S.load('/nonexistent/libcsa2.so')\n"
+            "except S.Csa2Error as e:\n"
+            "    print('raised:', e)\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.startswith("raised:") and "not found" in r.stdout
