@@ -436,7 +436,58 @@ def run_kernel_id():
     return h.hexdigest()[:16]
 
 
+def parse_cpulist(txt):
+    """CPU ids of a sysfs cpulist ("0-3,8,10-11")."""
+    cpus = set()
+    for part in txt.strip().split(","):
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        elif part:
+            cpus.add(int(part))
+    return cpus
+
+
+def gpu_local_cpus(dev_index):
+    """The CPUs local to the GPU's PCI device, within this thread's allowed
+    set; empty when unknown."""
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(dev_index)
+        addr = "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        with open("/sys/bus/pci/devices/%s/local_cpulist" % addr) as f:
+            return parse_cpulist(f.read()) & os.sched_getaffinity(0)
+    except Exception:
+        return set()
+
+
 def bench_e2e(args, w, run, dev, rank, world):
+    """The end-to-end leg with the issuing thread bound to the GPU-local CPUs
+    while it allocates the pinned host buffers and runs (the pages land on
+    that NUMA node), then unbound again."""
+    old = os.sched_getaffinity(0)
+    local = gpu_local_cpus(dev.index or 0)
+    bound = bool(local) and local != old
+    if bound:
+        try:
+            os.sched_setaffinity(0, local)
+        except OSError:
+            bound = False
+    try:
+        r = _bench_e2e(args, w, run, dev, rank, world)
+    finally:
+        if bound:
+            os.sched_setaffinity(0, old)
+    if bound:
+        r["host_cpus"] = "bound to the %d GPU-local CPUs of %d" % (len(local), len(old))
+    elif local:
+        r["host_cpus"] = "all %d allowed CPUs are GPU-local" % len(old)
+    else:
+        r["host_cpus"] = "GPU locality unknown: unbound"
+    return r
+
+
+def _bench_e2e(args, w, run, dev, rank, world):
     """Same step through the same calls, inputs from pinned host memory and the
     step's outputs read back, every step, copies inside the timed region.
 

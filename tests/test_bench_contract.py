@@ -41,3 +41,15 @@ def test_reference_arm_other_ranks_exit_without_work():
              LOCAL_RANK="1")
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_cpulist_parsing_and_unknown_locality():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.parse_cpulist("0-3,8,10-11\n") == {0, 1, 2, 3, 8, 10, 11}
+    assert bench.parse_cpulist("72-143") == set(range(72, 144))
+    assert bench.parse_cpulist("") == set()
+    # without a GPU the locality is unknown and nothing is bound
+    import torch
+    if not torch.cuda.is_available():
+        assert bench.gpu_local_cpus(0) == set()
