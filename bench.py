@@ -369,16 +369,165 @@ def bench_quant(args, w, stream, flush, hbm):
     return {"kernel": "csa2_quantize_rows", "peak_gbs": hbm, "cases": cases}
 
 
+def visible_entries(batch):
+    """Per query: entries its position sees, n_vis = floor((t + 1) / m), capped
+    by the entries stored for its request."""
+    import torch
+    t = batch["q_pos"].to(torch.int64)
+    r = batch["q_req"].to(torch.int64)
+    nv = torch.div(t + 1, int(batch["ratio"]), rounding_mode="floor")
+    return torch.minimum(nv, batch["kv_len"].to(torch.int64)[r])
+
+
+def window_rows(batch, win_lo, window):
+    """Per query: stored SWA rows of its window [max(win_lo, t - window + 1, 0), t]."""
+    import torch
+    t = batch["q_pos"].to(torch.int64)
+    r = batch["q_req"].to(torch.int64)
+    lo = (t - window + 1).clamp(min=0)
+    if win_lo is not None:
+        lo = torch.maximum(lo, win_lo.to(torch.int64))
+    p0 = batch["swa_pos0"].to(torch.int64)[r]
+    pn = batch["swa_len"].to(torch.int64)[r]
+    return (torch.minimum(t, p0 + pn - 1) - torch.maximum(lo, p0) + 1).clamp(min=0)
+
+
+def pool_pairs(batch, blocks, block):
+    """Per query: visible entries of its candidate blocks (-1 padded)."""
+    import torch
+    nv = visible_entries(batch)
+    b = blocks.to(torch.int64)
+    cnt = (nv[:, None] - b * block).clamp(min=0, max=block)
+    return torch.where(b >= 0, cnt, torch.zeros_like(cnt)).sum(dim=1)
+
+
+def attn_launch_bytes(batch, idx, win_lo, window, n_heads, sel_row_bytes=ROW_BYTES):
+    """The method's own bytes of one attention launch: valid selected rows and
+    stored window rows (576 B each), Q and O (bf16), the index row (int32) and
+    the lse (fp32) of every query."""
+    import torch
+    nq = int(batch["num_q"])
+    n_sel = 0
+    k = 0
+    if idx is not None:
+        k = int(idx.shape[1])
+        nv = visible_entries(batch)
+        n_sel = int(((idx >= 0) & (idx.to(torch.int64) < nv[:, None])).sum())
+    n_win = int(window_rows(batch, win_lo, window).sum())
+    return n_sel * sel_row_bytes + n_win * ROW_BYTES + nq * (n_heads * 512 * 2 * 2 + k * 4 +
+                                                             n_heads * 4)
+
+
+def index_score_flops(pairs, n_idx_heads, head_dim=128):
+    """Multiply-adds of the per-head dots, as flops (the ReLU-weighted head sum
+    is not counted)."""
+    return 2 * int(pairs) * n_idx_heads * head_dim
+
+
+def kernel_breakdown(name, w, runs, flush, hbm_gbs, tflops_peak, reps=3):
+    """Each launch of one workload's sequence timed alone (events, L2 flushed
+    before each, mean of `reps`), with the method's own bytes (attention) or
+    flops (index score) against the measured peaks."""
+    import torch
+
+    def timed(fn):
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ts) / len(ts)
+
+    out = []
+
+    def score(run, layer, blocks=None):
+        b = run.batches[layer]
+        if blocks is None:
+            ms = timed(lambda: run.score_full(layer))
+            pairs = int(visible_entries(b).sum())
+        else:
+            ms = timed(lambda: run.score_pool(layer, blocks))
+            pairs = int(pool_pairs(b, blocks, w.block).sum())
+        fl = index_score_flops(pairs, w.n_idx_heads)
+        out.append({"kernel": "index_score", "layer": layer, "pool": blocks is not None,
+                    "avg_launch_ms": round(ms, 4), "pairs": pairs, "flops": fl,
+                    "achieved_tflops": round(fl / (ms * 1e-3) / 1e12, 1),
+                    "frac_of_f16_peak": round(fl / (ms * 1e-3) / 1e12 / tflops_peak, 3)})
+
+    def select(run, layer, fn):
+        out.append({"kernel": "topk", "layer": layer, "avg_launch_ms": round(timed(fn), 4)})
+
+    def attend(run, layer, idx, win_lo):
+        b = run.batches[layer]
+        if win_lo is None and w.layers[layer].win_lo is not None:
+            win_lo = run._lt(layer, "win_lo")
+        ms = timed(lambda: run.attend(layer, idx, win_lo))
+        by = attn_launch_bytes(b, idx, win_lo, w.window, w.n_heads)
+        out.append({"kernel": "sparse_swa_attn", "layer": layer, "avg_launch_ms": round(ms, 4),
+                    "algorithmic_bytes": by, "achieved_gbs": round(by / (ms * 1e-3) / 1e9, 1),
+                    "frac_of_hbm": round(by / (ms * 1e-3) / 1e9 / hbm_gbs, 3)})
+
+    if name == "c5_ragged_mixed":
+        run_ri, run_ru, given = runs
+        score(run_ri, "mixed")
+        select(run_ri, "mixed", lambda: run_ri.select("mixed", run_ri.scores))
+        attend(run_ri, "mixed", run_ri.idx["mixed"], None)
+        attend(run_ru, "mixed", given, None)
+    elif name == "c2_decoder_replay":
+        run, = runs
+        score(run, "L20")
+        select(run, "L20", lambda: run.select_candidates("L20", run.scores))
+        attend(run, "L20", run.idx["L20"], None)
+        score(run, "L21", run.blocks)
+        select(run, "L21", lambda: run.select("L21", run.pool_scores, run.blocks))
+        attend(run, "L21", run.idx["L21"], run.tail_win_lo)
+        attend(run, "L22", run.idx["L21"], run.tail_win_lo)
+    elif name == "c4_hierarchical":
+        run, = runs
+        score(run, "L20")
+        select(run, "L20", lambda: run.select_candidates("L20", run.scores))
+        attend(run, "L20", run.idx["L20"], None)
+        score(run, "L21", run.blocks)
+        select(run, "L21", lambda: run.select("L21", run.pool_scores, run.blocks))
+        attend(run, "L21", run.idx["L21"], None)
+    else:
+        run, = runs
+        score(run, "full")
+        select(run, "full", lambda: run.select("full", run.scores))
+        attend(run, "full", run.idx["full"], None)
+    summary = {}
+    for kind, unit, peak, key in (("sparse_swa_attn", "algorithmic_bytes", hbm_gbs * 1e9,
+                                   "attention_frac_of_hbm"),
+                                  ("index_score", "flops", tflops_peak * 1e12,
+                                   "index_score_frac_of_f16_peak")):
+        ks = [k for k in out if k["kernel"] == kind]
+        if ks:
+            tot = sum(k[unit] for k in ks) / (sum(k["avg_launch_ms"] for k in ks) * 1e-3)
+            summary[key] = round(tot / peak, 3)
+    return out, summary
+
+
 def bench_configs(args):
     """Layer-queries/s of each named workload's call sequence (the sequences the
     full-size parity tests run), one JSON line per workload.  Events around each
-    sequence, L2 flushed before each, 2 warm-up and 5 timed repetitions."""
+    sequence, L2 flushed before each, 2 warm-up and 5 timed repetitions.  Then
+    every launch of the sequence timed alone, with the attention launches'
+    fraction of the HBM peak and the index-score launches' fraction of the
+    f16 tensor peak (the method's own bytes and flops)."""
     import torch
     from sparse_attention_prefill_gb300 import synth
     from sparse_attention_prefill_gb300.layer import LayerRunner
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    hbm, _, peaks_src = measured_peaks()
+    # each launch is timed alone: the burst tensor peak
+    tflops = (json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"]
+              if peaks_src == "measured" else 1900.0)
     for name in synth.CONFIG_NAMES:
         w = synth.config(name, dev, args.seed)
         if name == "c5_ragged_mixed":
@@ -415,9 +564,12 @@ def bench_configs(args):
         torch.cuda.synchronize()
         assert all(int(d.item()) == 0 for d in d_errs), name
         ms = sum(a.elapsed_time(b) for a, b in ts) / len(ts)
+        runs = (run_ri, run_ru, given) if name == "c5_ragged_mixed" else (run,)
+        kernels, summary = kernel_breakdown(name, w, runs, flush, hbm, tflops)
         print(json.dumps({"workload": name, "query_rows": rows, "layers": layers,
                           "ms_per_sequence": round(ms, 4),
-                          "layer_queries_per_s": round(layers * rows / (ms * 1e-3), 1)}),
+                          "layer_queries_per_s": round(layers * rows / (ms * 1e-3), 1),
+                          **summary, "peaks": peaks_src, "kernels": kernels}),
               flush=True)
         del w
         torch.cuda.empty_cache()

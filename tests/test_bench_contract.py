@@ -53,3 +53,57 @@ def test_cpulist_parsing_and_unknown_locality():
     import torch
     if not torch.cuda.is_available():
         assert bench.gpu_local_cpus(0) == set()
+
+
+def _tiny_batch(rng, nq=40, nreq=3, ratio=2):
+    import torch
+    kv_len = torch.tensor(rng.integers(0, 300, nreq), dtype=torch.int64)
+    swa_pos0 = torch.tensor(rng.integers(0, 200, nreq), dtype=torch.int64)
+    swa_len = torch.tensor(rng.integers(0, 300, nreq), dtype=torch.int64)
+    q_req = torch.tensor(rng.integers(0, nreq, nq), dtype=torch.int32)
+    q_pos = torch.tensor(rng.integers(0, 600, nq), dtype=torch.int64)
+    return dict(num_q=nq, num_req=nreq, ratio=ratio, q_req=q_req, q_pos=q_pos,
+                kv_start=torch.zeros(nreq, dtype=torch.int64), kv_len=kv_len,
+                swa_start=torch.zeros(nreq, dtype=torch.int64), swa_pos0=swa_pos0,
+                swa_len=swa_len)
+
+
+def test_roofline_counts_match_brute_force():
+    """The per-launch accounting of `bench.py --configs` (visible entries,
+    stored window rows, pool pairs, attention bytes, index flops) against
+    plain loops."""
+    import numpy as np
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    rng = np.random.default_rng(7)
+    for ratio in (1, 2):
+        b = _tiny_batch(rng, ratio=ratio)
+        nq = b["num_q"]
+        win_lo = torch.tensor(rng.integers(0, 500, nq), dtype=torch.int64)
+        window, block, k, heads = 128, 8, 16, 4
+        blocks = torch.full((nq, 10), -1, dtype=torch.int32)
+        idx = torch.tensor(rng.integers(-1, 400, (nq, k)), dtype=torch.int32)
+        nv_ref, win_ref, pool_ref, sel_ref = [], [], [], 0
+        for q in range(nq):
+            r, t = int(b["q_req"][q]), int(b["q_pos"][q])
+            nv = min((t + 1) // ratio, int(b["kv_len"][r]))
+            nv_ref.append(nv)
+            lo = max(int(win_lo[q]), t - window + 1, 0)
+            p0, pn = int(b["swa_pos0"][r]), int(b["swa_len"][r])
+            win_ref.append(sum(1 for p in range(lo, t + 1) if p0 <= p < p0 + pn))
+            nb = int(rng.integers(0, 11))
+            chosen = sorted(rng.choice(max(1, (nv + block - 1) // block + 2), size=min(
+                nb, max(1, (nv + block - 1) // block + 2)), replace=False).tolist())
+            blocks[q, :len(chosen)] = torch.tensor(chosen, dtype=torch.int32)
+            pool_ref.append(sum(1 for c in chosen for j in range(c * block, c * block + block)
+                                if j < nv))
+            sel_ref += sum(1 for j in idx[q].tolist() if 0 <= j < nv)
+        assert bench.visible_entries(b).tolist() == nv_ref
+        assert bench.window_rows(b, win_lo, window).tolist() == win_ref
+        assert bench.pool_pairs(b, blocks, block).tolist() == pool_ref
+        want = sel_ref * 576 + sum(win_ref) * 576 + nq * (heads * 512 * 4 + k * 4 + heads * 4)
+        assert bench.attn_launch_bytes(b, idx, win_lo, window, heads) == want
+        assert bench.attn_launch_bytes(b, None, None, window, heads) == (
+            int(bench.window_rows(b, None, window).sum()) * 576 + nq * (heads * 512 * 4 + heads * 4))
+    assert bench.index_score_flops(10, 32) == 2 * 10 * 32 * 128
