@@ -875,18 +875,18 @@ using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t,
                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// looked up once; the initialisation of a function-local static is
+// thread-safe, so concurrent first calls all see the finished lookup
 EncodeTiled encode_tiled() {
-  static EncodeTiled fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  static const EncodeTiled fn = []() -> EncodeTiled {
     void *p = nullptr;
     cudaDriverEntryPointQueryResult res;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &res) == cudaSuccess &&
         res == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiled>(p);
-  }
+      return reinterpret_cast<EncodeTiled>(p);
+    return nullptr;
+  }();
   return fn;
 }
 
