@@ -673,21 +673,27 @@ int topk_launch(const Batch &b, const float *scores, int64_t ld, int k,
   const int64_t nblk = (ld + block - 1) / block;
   const size_t smem_b = (size_t)(nblk < kSmemKeys ? (nblk > 0 ? nblk : 1) : kSmemKeys) *
                         sizeof(uint32_t);
-  auto launch = [&](auto kern, int nt, int64_t staged) {
+  // Each kernel's shared-memory attribute is its largest request (the most
+  // keys it stages plus the most candidate blocks), the same value on every
+  // call, so that concurrent callers never lower it under another's launch.
+  auto launch = [&](auto kern, int nt, int64_t staged, int64_t staged_max) {
     const size_t smem = (size_t)(staged + (cand_blocks ? max_blocks : 0)) * sizeof(uint32_t);
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const size_t smem_max = (size_t)(staged_max + kMaxSortBlocks) * sizeof(uint32_t);
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
     kern<<<b.num_q, nt, smem, st>>>(b, scores, ld, k, cand_blocks, block, max_blocks, idx, count,
                                     d_err, staged);
   };
-  if (row_cap <= 256 * 4) launch(topk_kernel<256, 4>, 256, 0);
-  else if (row_cap <= 256 * 8) launch(topk_kernel<256, 8>, 256, 0);
-  else if (row_cap <= 256 * 16) launch(topk_kernel<256, 16>, 256, 0);
-  else if (row_cap <= 256 * 32) launch(topk_kernel<256, 32>, 256, 0);
-  else if (row_cap <= 256 * 64) launch(topk_kernel<256, 64>, 256, 0);
-  else launch(topk_kernel<kThreads, 32>, kThreads, row_cap < kSmemKeys ? row_cap : kSmemKeys);
+  if (row_cap <= 256 * 4) launch(topk_kernel<256, 4>, 256, 0, 0);
+  else if (row_cap <= 256 * 8) launch(topk_kernel<256, 8>, 256, 0, 0);
+  else if (row_cap <= 256 * 16) launch(topk_kernel<256, 16>, 256, 0, 0);
+  else if (row_cap <= 256 * 32) launch(topk_kernel<256, 32>, 256, 0, 0);
+  else if (row_cap <= 256 * 64) launch(topk_kernel<256, 64>, 256, 0, 0);
+  else
+    launch(topk_kernel<kThreads, 32>, kThreads, row_cap < kSmemKeys ? row_cap : kSmemKeys,
+           kSmemKeys);
   if (blocks_out) {
     cudaFuncSetAttribute(candidate_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)smem_b);
+                         (int)(kSmemKeys * sizeof(uint32_t)));
     candidate_blocks_kernel<<<b.num_q, kThreads, smem_b, st>>>(
         b, scores, ld, block, max_blocks, blocks_out, nblocks_out,
         nblk < kSmemKeys ? nblk : (int64_t)kSmemKeys);
