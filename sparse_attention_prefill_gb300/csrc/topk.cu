@@ -121,6 +121,11 @@ __device__ __forceinline__ void sweep(const Keys &keys, int64_t n, F f) {
 template <int NT, class Keys, class Emit>
 __device__ uint32_t select_topk(const Keys &keys, int64_t n, uint32_t k, SelectShared<NT> &sh,
                                 Emit emit) {
+  // k = 0 (candidate ranking with a one-block budget: only the latest block
+  // is kept) selects nothing; the radix search below assumes k >= 1, since
+  // with k = 0 no bin would ever hold the k-th key and the threshold would
+  // stay at 0.  k is uniform over the block, so every thread returns here.
+  if (k == 0u) return 0u;
   // radix select of the k-th largest key; the first pass also counts the
   // eligible keys (the histogram total)
   if (threadIdx.x == 0) {

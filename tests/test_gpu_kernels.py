@@ -225,6 +225,10 @@ def test_topk_pool_mode_bit_exact():
     ([16383, 16384, 16385, 16393, 131072, 130561, 9, 1, 0], 8, 2048),
     ([23, 22, 9, 8, 7, 3], 2, 4),
     ([50000, 400001], 8, 4096),
+    # one- and two-block budgets: only the latest block, or it and the best
+    # other block (rows longer than the 4096-block ranking buffer included)
+    ([40000, 33000, 17, 9, 8, 1, 0], 8, 1),
+    ([40000, 33000, 17, 9, 8, 1, 0], 8, 2),
 ])
 def test_candidates_bit_exact(n_vis_list, bsz, nb_max):
     rng = np.random.default_rng(len(n_vis_list) + bsz)

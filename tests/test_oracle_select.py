@@ -86,10 +86,12 @@ def _brute_blocks(row, n_vis, bsz, nb_max):
     return sorted([b for _, b in bm[:nb_max - 1]] + [nb - 1])
 
 
-@pytest.mark.parametrize("seed", range(6))
-def test_candidates_brute_force_small_pool(seed):
+@pytest.mark.parametrize("seed,nb_max", [(s, 4) for s in range(6)] + [(6, 1), (7, 2)])
+def test_candidates_brute_force_small_pool(seed, nb_max):
+    """A one-block budget keeps only the latest block; two keep it plus the
+    best earlier block."""
     rng = np.random.default_rng(seed)
-    bsz, nb_max, n = 2, 4, 23
+    bsz, n = 2, 23
     s = np.round(rng.standard_normal((n, n)) * 2) / 2
     s = s.astype(np.float32)
     q_pos = list(range(n))
