@@ -68,11 +68,12 @@ def topk_sets_match(gpu_idx, gpu_count, ref_idx, ref_count):
 def topk_near_tie_ok(gpu_idx, gpu_count, ref_idx, ref_count, ref_scores, entry_of_col=None,
                      rel=1e-3):
     """End-to-end top-K rule: sets equal except for swaps among entries whose
-    oracle scores lie within rel * |s_k| of the oracle's k-th score."""
+    oracle scores lie within rel * |s_k| of the oracle's k-th score.  Returns
+    the positions of the rows whose sets differ (each one checked)."""
     gi = gpu_idx.detach().cpu().numpy()
     gc = gpu_count.detach().cpu().numpy()
     assert (gc == ref_count).all()
-    swaps = 0
+    rows = []
     for q in range(gi.shape[0]):
         c = int(ref_count[q])
         a, b = set(gi[q, :c].tolist()), set(ref_idx[q, :c].tolist())
@@ -84,5 +85,45 @@ def topk_near_tie_ok(gpu_idx, gpu_count, ref_idx, ref_count, ref_scores, entry_o
         sk = min(row[col(e)] for e in b)
         for e in diff:
             assert abs(row[col(e)] - sk) <= rel * abs(sk) + 1e-30, (q, e, row[col(e)], sk)
-        swaps += len(diff) // 2
-    return swaps
+        rows.append(q)
+    return rows
+
+
+def block_maxima(row: np.ndarray, n_vis: int, block: int) -> np.ndarray:
+    """Maximum oracle score of each block of `block` entries over the first
+    n_vis entries of a full-visible score row (NaN ignored)."""
+    nb = -(-n_vis // block)
+    r = np.full(nb * block, -np.inf)
+    v = row[:n_vis].astype(np.float64)
+    r[:n_vis] = np.where(np.isnan(v), -np.inf, v)
+    return r.reshape(nb, block).max(1) if nb else r
+
+
+def pool_near_tie_rows(gpu_blocks, gpu_nblocks, ref_blocks, ref_nblocks, ref_scores, block,
+                       rel=1e-3):
+    """End-to-end candidate pools: bit-exact per row.  A row may differ only
+    when every block in the symmetric difference has an oracle block maximum
+    within rel * |m_k| of m_k, the lowest block maximum the oracle kept among
+    the ranked blocks (every block but the latest); the latest block must be
+    in both pools.  `ref_scores` are the oracle's full-visible scores of the
+    same rows (columns = entries; unwritten columns NaN).  Returns the
+    positions of the rows that differ."""
+    gb = npy(gpu_blocks) if torch.is_tensor(gpu_blocks) else gpu_blocks
+    gn = npy(gpu_nblocks) if torch.is_tensor(gpu_nblocks) else gpu_nblocks
+    assert (gn == ref_nblocks).all(), np.nonzero(gn != ref_nblocks)[0][:10]
+    rows = []
+    for q in range(gb.shape[0]):
+        if (gb[q] == ref_blocks[q]).all():
+            continue
+        n = int(ref_nblocks[q])
+        assert (gb[q, n:] == -1).all() and (np.diff(gb[q, :n]) > 0).all(), q
+        n_vis = int((~np.isnan(ref_scores[q])).sum())
+        latest = -(-n_vis // block) - 1
+        a, b = set(gb[q, :n].tolist()), set(ref_blocks[q, :n].tolist())
+        assert latest in a and latest in b, q
+        bm = block_maxima(ref_scores[q], n_vis, block)
+        mk = min(bm[x] for x in b if x != latest)
+        for x in a ^ b:
+            assert abs(bm[x] - mk) <= rel * abs(mk) + 1e-30, (q, x, bm[x], mk)
+        rows.append(q)
+    return rows

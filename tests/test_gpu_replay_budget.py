@@ -51,7 +51,8 @@ def test_decoder_tail_step_replay_budget(replay):
         assert (pos - lo >= 127).any()
     rows = torch.arange(w.num_q, device=DEV)
     win = run.tail_win_lo
-    _, blocks = _layer_parity(w, run, "L20", rows, "source")
-    idx21, _ = _layer_parity(w, run, "L21", rows, "reindex", pool=blocks, win_lo=win)
-    _layer_parity(w, run, "L22", rows, "reuse", given_idx=idx21, win_lo=win,
+    _, blocks, pool_rows = _layer_parity(w, run, "L20", rows, "source", label="R=%d" % replay)
+    idx21, _, just21 = _layer_parity(w, run, "L21", rows, "reindex", pool=blocks, win_lo=win,
+                                     justified=pool_rows, label="R=%d" % replay)
+    _layer_parity(w, run, "L22", rows, "reuse", given_idx=idx21, win_lo=win, justified=just21,
                   chain_idx=run.idx["L21"])
