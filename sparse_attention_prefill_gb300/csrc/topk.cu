@@ -16,9 +16,13 @@
 //    memory (typically ~1.1k); an 8-bit radix search finds the exact k-th key
 //    on that list alone.  A guess that lists fewer than k keys or more than
 //    the list holds falls back to the same search over the whole row.
-//  - Longer rows: a 4-pass radix select over the row staged in shared memory
-//    (or re-read from L2), then keys > T emitted directly and the keys equal
-//    to T taken in position order by a block-wide ordered scan.
+//  - Longer rows (staged in shared memory, or re-read from L2): the same kind
+//    of guess from every 16th key, one sweep that lists the keys at or above
+//    it (up to 4096, with positions), and the exact search on the list; ties
+//    at the k-th key by a second radix over inverted positions.  A guess that
+//    misses falls back to a 4-pass radix select over the whole row, keys > T
+//    emitted directly and the keys equal to T taken in position order by a
+//    block-wide ordered scan.
 // Every sweep over a row loads several elements per thread before using any,
 // so that the loads overlap.  The same selection core ranks candidate blocks
 // by block maximum, and the chosen blocks are sorted ascending with a
@@ -545,6 +549,135 @@ __device__ void row_geometry(const Batch &b, int q, const int32_t *cand_blocks, 
 }
 
 // minimum residency chosen so the key registers do not spill
+
+// Long rows (past the register path): a threshold guess from the moments of
+// every 16th key, then one sweep that lists the keys at or above it (up to
+// kListCap, with their positions).  With between k and kListCap keys listed
+// the exact search runs on the list: the k-th key by radix, and the keys equal
+// to it, if only some are taken, by a second radix over their inverted
+// positions (lowest positions first).  Returns false, having emitted nothing,
+// when the guess misses; the caller then searches the whole row.
+template <int NT, class Keys, class Emit>
+__device__ bool select_topk_listed(const Keys &keys, int64_t n, uint32_t k, RegShared<NT> &sh,
+                                   Emit emit) {
+  constexpr int kS = 16;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  uint32_t s_cnt = 0, f_cnt = 0;
+  float f_sum = 0.f, f_sq = 0.f;
+#pragma unroll 4
+  for (int64_t i = (int64_t)t * kS; i < n; i += (int64_t)NT * kS) {
+    const uint32_t x = keys.key(i, keys.raw(i));
+    if (x != 0u) {
+      ++s_cnt;
+      const float f = __uint_as_float((x & 0x80000000u) ? x ^ 0x80000000u : ~x);
+      if (fabsf(f) <= 3.0e38f) {
+        ++f_cnt;
+        f_sum += f;
+        f_sq += f * f;
+      }
+    }
+  }
+  s_cnt = __reduce_add_sync(0xffffffffu, s_cnt);
+  f_cnt = __reduce_add_sync(0xffffffffu, f_cnt);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    f_sum += __shfl_xor_sync(0xffffffffu, f_sum, o);
+    f_sq += __shfl_xor_sync(0xffffffffu, f_sq, o);
+  }
+  if (lane == 0) {
+    sh.red[0][warp] = s_cnt;
+    sh.red[3][warp] = f_cnt;
+    sh.red[4][warp] = __float_as_uint(f_sum);
+    sh.red[5][warp] = __float_as_uint(f_sq);
+  }
+  for (int i = t; i < 256; i += NT) sh.hist[i] = 0;
+  if (t == 0) sh.out_count = 0;
+  __syncthreads();
+  s_cnt = 0;
+  f_cnt = 0;
+  f_sum = 0.f;
+  f_sq = 0.f;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    s_cnt += sh.red[0][w];
+    f_cnt += sh.red[3][w];
+    f_sum += __uint_as_float(sh.red[4][w]);
+    f_sq += __uint_as_float(sh.red[5][w]);
+  }
+  // the same guess as the register path, with the eligible count estimated
+  // from the sample (any guess is safe)
+  if (f_cnt <= 1) return false;
+  const float n_elig = (float)s_cnt * (float)kS;
+  const float mean = f_sum / (float)f_cnt;
+  const float sd = sqrtf(fmaxf(f_sq / (float)f_cnt - mean * mean, 0.f));
+  const float p = (float)(2u * k + 64u) / n_elig;
+  if (!(p < 1.f) || !(sd > 0.f)) return false;
+  const uint32_t t_est = score_key(mean + 1.41421356f * erfcinvf(2.f * p) * sd);
+  if (t_est == 0u) return false;
+  // list the keys >= t_est; the counter runs on past the capacity
+  uint32_t mx = 0;
+  sweep<NT>(keys, n, [&](int64_t i, uint32_t x) {
+    const bool take = x != 0u && x >= t_est;
+    const uint32_t slot = warp_reserve(take, &sh.out_count);
+    if (take && slot < (uint32_t)kListCap) {
+      sh.list_key[slot] = x;
+      sh.list_pos[slot] = (int32_t)i;
+    }
+    mx = max(mx, take ? x : 0u);
+  });
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (lane == 0) sh.red[2][warp] = mx;
+  __syncthreads();
+  const uint32_t n_list = sh.out_count;
+  mx = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) mx = max(mx, sh.red[2][w]);
+  __syncthreads();
+  if (t == 0) sh.out_count = 0;
+  __syncthreads();
+  if (n_list < k || n_list > (uint32_t)kListCap) return false;
+  uint32_t prefix, rem;
+  bool whole;
+  radix_kth<NT>(
+      [&](auto f) {
+        for (int i = t; i < (int)n_list; i += NT) f(sh.list_key[i]);
+      },
+      t_est, mx, k, sh, prefix, rem, whole);
+  const uint32_t lo = whole ? prefix : prefix + 1u;
+  for (int i0 = 0; i0 < (int)n_list; i0 += NT) {
+    const int i = i0 + t;
+    const uint32_t x = i < (int)n_list ? sh.list_key[i] : 0u;
+    const bool take = x != 0u && x >= lo;
+    const uint32_t slot = warp_reserve(take, &sh.out_count);
+    if (take) emit(sh.list_pos[i], slot);
+  }
+  if (!whole) {
+    // the rem lowest positions among the listed keys equal to prefix:
+    // largest inverted positions (positions are below 2^31, so these keys are
+    // nonzero and distinct)
+    auto inv = [&](int i) -> uint32_t {
+      return sh.list_key[i] == prefix ? 0xffffffffu - (uint32_t)sh.list_pos[i] : 0u;
+    };
+    uint32_t p2, rem2;
+    bool whole2;
+    radix_kth<NT>(
+        [&](auto f) {
+          for (int i = t; i < (int)n_list; i += NT) f(inv(i));
+        },
+        0x80000000u, 0xffffffffu, rem, sh, p2, rem2, whole2);
+    const uint32_t lo2 = whole2 ? p2 : p2 + 1u;
+    for (int i0 = 0; i0 < (int)n_list; i0 += NT) {
+      const int i = i0 + t;
+      const uint32_t y = i < (int)n_list ? inv(i) : 0u;
+      const bool take = y != 0u && (y >= lo2 || (!whole2 && y == p2));
+      const uint32_t slot = warp_reserve(take, &sh.out_count);
+      if (take) emit(sh.list_pos[i], slot);
+    }
+  }
+  __syncthreads();
+  return true;
+}
+
 template <int NT, int KPT>
 __global__ void __launch_bounds__(NT, NT >= 512 ? 1 : KPT >= 64 ? 2 : KPT >= 32 ? 3 : 4)
 topk_kernel(Batch b, const float *__restrict__ scores, int64_t ld, int k,
@@ -593,9 +726,15 @@ topk_kernel(Batch b, const float *__restrict__ scores, int64_t ld, int k,
       if (s < row_len) skeys[s] = x;
     });
     __syncthreads();
-    got = select_topk<NT>(SmemKeys{skeys}, row_len, (uint32_t)k, sh, emit);
+    if (select_topk_listed<NT>(SmemKeys{skeys}, row_len, (uint32_t)k, rsh, emit))
+      got = (uint32_t)k;
+    else
+      got = select_topk<NT>(SmemKeys{skeys}, row_len, (uint32_t)k, sh, emit);
   } else {
-    got = select_topk<NT>(view, row_len, (uint32_t)k, sh, emit);
+    if (select_topk_listed<NT>(view, row_len, (uint32_t)k, rsh, emit))
+      got = (uint32_t)k;
+    else
+      got = select_topk<NT>(view, row_len, (uint32_t)k, sh, emit);
   }
   for (int i = (int)got + threadIdx.x; i < k; i += NT) out[i] = -1;
   if (threadIdx.x == 0) count[q] = (int32_t)got;
