@@ -7,8 +7,9 @@
  *  - Every pointer argument is DEVICE memory allocated and owned by the caller,
  *    except `const csa2_batch *b`, which is a host struct holding device
  *    pointers, and is read during the call only.  The library allocates
- *    nothing and keeps no state between calls; results are written only to the
- *    output arrays named below.
+ *    nothing and keeps no state between calls (the one exception is the
+ *    diagnostic wait bound of csa2_set_wait_limit_ns); results are written
+ *    only to the output arrays named below.
  *  - Work is enqueued on `stream` (0 = legacy default stream); no entry point
  *    synchronises the host.  Calls are thread-safe.
  *  - Return value: CSA2_OK, or a status describing an argument the host could
@@ -61,7 +62,7 @@ typedef struct CUstream_st *csa2_stream_t; /* same object as cudaStream_t */
 #define CSA2_ERR_INVALID_ARG 1 /* host-checked argument error; nothing launched */
 #define CSA2_ERR_UNSUPPORTED 2 /* valid request this build does not implement */
 #define CSA2_ERR_CUDA 3        /* a kernel launch failed */
-#define CSA2_ERR_TIMEOUT 4     /* reserved */
+#define CSA2_ERR_TIMEOUT 4     /* reserved (device waits report CSA2_DERR_TIMEOUT) */
 
 /* data-error bits ORed into *d_err */
 #define CSA2_DERR_RANGE_IDX 1     /* a selected index outside [0, n_vis) or past kv_len */
@@ -110,6 +111,18 @@ typedef struct csa2_batch {
 
 /* Human-readable name of a status code (static storage). */
 CSA2_API const char *csa2_status_string(int status);
+
+/* Bound on every pipeline wait inside the tensor-core kernels (index score,
+ * attention), in nanoseconds of the GPU's global timer, for launches issued
+ * after the call from any thread; 0 restores the default of 2 s.  When a wait
+ * runs out the kernel raises CSA2_DERR_TIMEOUT, stops its pipeline, waits
+ * (for at most 2 s) for the tensor-core work and copies it has in flight,
+ * frees its tensor memory and returns: the outputs of that launch are
+ * undefined, the CUDA context stays usable and later launches are unaffected.
+ * A negative test shortens the bound so that waits run out; the pages ask
+ * that such failures be reported without taking the serving process down
+ * ([TAIL] sec. 2.7).  Always returns CSA2_OK. */
+CSA2_API int csa2_set_wait_limit_ns(uint64_t ns);
 
 /* ---------------------------------------------------------------------------
  * a1. Decoder bounded-replay tail layout   [TAIL] sec. 2.1, 2.2, 2.5, 2.6 and

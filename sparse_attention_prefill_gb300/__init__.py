@@ -29,7 +29,7 @@ FMT_FP8_B32, FMT_FP4KV, FMT_MXFP4 = 1, 2, 3
 EXPORTED = ("csa2_status_string", "csa2_tail_layout", "csa2_index_score", "csa2_topk",
             "csa2_topk_candidates", "csa2_sparse_swa_attn", "csa2_sparse_swa_attn_fp4kv",
             "csa2_encoder_replay_layout", "csa2_rows_gather", "csa2_rows_scatter",
-            "csa2_quantize_rows")
+            "csa2_quantize_rows", "csa2_set_wait_limit_ns")
 
 
 class Csa2Error(RuntimeError):
@@ -73,10 +73,20 @@ def load(path: Optional[str] = None):
     lib.csa2_rows_gather.argtypes = [vp, i64, vp, vp, i64, vp, i64, vp, vp]
     lib.csa2_rows_scatter.argtypes = [vp, i64, vp, vp, vp, i64, i64, vp, vp]
     lib.csa2_quantize_rows.argtypes = [i32, i64, vp, i32, vp, vp, vp, i64, vp, vp]
+    lib.csa2_set_wait_limit_ns.argtypes = [C.c_uint64]
     for name in EXPORTED[1:]:
         getattr(lib, name).restype = C.c_int
     _lib = lib
     return lib
+
+
+def csa2_set_wait_limit_ns(ns: int) -> int:
+    """Bound on the tensor-core kernels' pipeline waits for later launches
+    (0 restores the default, 2 s)."""
+    return load().csa2_set_wait_limit_ns(int(ns))
+
+
+set_wait_limit_ns = csa2_set_wait_limit_ns
 
 
 def status_string(status: int) -> str:

@@ -10,6 +10,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libcsa2.so")
+PROBE_SRC = os.path.join(HERE, "probe", "mma_peak.cu")
+PROBE_LIB = os.path.join(OUT_DIR, "libcsa2_probe.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden", "--expt-relaxed-constexpr",
@@ -30,6 +32,23 @@ def _sources():
 def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + [
         os.path.join(ROOT, "include", "csa2.h"), os.path.abspath(__file__)]
+
+
+def build_probe(force: bool = False) -> str:
+    """Compile the tensor-core throughput probe (a measurement tool kept out of
+    libcsa2) into its own shared library."""
+    deps = [PROBE_SRC, os.path.join(CSRC, "tcgen05.cuh")]
+    if (not force and os.path.exists(PROBE_LIB)
+            and os.path.getmtime(PROBE_LIB) >= max(os.path.getmtime(p) for p in deps)):
+        return PROBE_LIB
+    os.makedirs(OUT_DIR, exist_ok=True)
+    tmp = PROBE_LIB + ".tmp.%d" % os.getpid()
+    cmd = [_nvcc(), *ARCH, *FLAGS, "-shared", "-cudart", "shared", PROBE_SRC, "-o", tmp]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError("nvcc failed on %s:\n%s%s" % (PROBE_SRC, res.stdout, res.stderr))
+    os.replace(tmp, PROBE_LIB)
+    return PROBE_LIB
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:

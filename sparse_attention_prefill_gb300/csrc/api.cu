@@ -15,6 +15,11 @@ extern "C" CSA2_API const char *csa2_status_string(int status) {
   }
 }
 
+extern "C" CSA2_API int csa2_set_wait_limit_ns(uint64_t ns) {
+  csa2::wait_limit_store().store(ns ? ns : csa2::kDefaultWaitNs, std::memory_order_relaxed);
+  return CSA2_OK;
+}
+
 extern "C" CSA2_API int csa2_index_score(const csa2_batch *b, int32_t n_heads, int32_t head_dim,
                                 const uint8_t *q_fp4, const float *q_scale, const float *head_w,
                                 const uint8_t *k_fp4, const float *k_scale,

@@ -37,8 +37,10 @@
 //               one step ahead; a chunk buffer is released in 32-row halves
 // The per-query row sums and maxima are reduced across a warp's lanes with a
 // reduce-scatter (five halving steps).
-// Every wait is bounded (about two seconds); on expiry the kernel raises
-// CSA2_DERR_TIMEOUT, drains and returns.
+// Every wait is bounded (two seconds unless csa2_set_wait_limit_ns says
+// otherwise); on expiry the kernel raises CSA2_DERR_TIMEOUT, drains its MMAs
+// and any Q copy in flight (each for at most two seconds), frees TMEM and
+// returns.
 #include <cuda.h>   // CUtensorMap (the encoder is reached through the runtime)
 
 #include "common.cuh"
@@ -82,7 +84,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;           // 2 x 64 (M = 64 layout)
 constexpr uint32_t kColO = 128;         // 4 x 64
 
-constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kWaitNs = 2000000000ull;   // drains (the pipeline waits take Params::wait_ns)
 constexpr int kDerrTimeout = 128;
 
 struct Misc {
@@ -91,6 +93,7 @@ struct Misc {
   uint64_t meta_full[2];
   int64_t meta[2][4];   // per query (ring of 2): selected rows, window rows, first SWA
                         // row, pool row of the request's entry 0
+  uint64_t wait_ns;     // bound on every pipeline wait
   uint32_t tmem_base;
   int abort;
   int votes[2][8];      // softmax warps: "a logit exceeded the reference", by chunk parity
@@ -119,7 +122,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Misc *m
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
     if (*(volatile int *)&ms->abort) return false;
-    if (globaltimer() - t0 > kWaitNs) {
+    if (globaltimer() - t0 > ms->wait_ns) {
       atomicExch(&ms->abort, 1);
       return false;
     }
@@ -211,6 +214,7 @@ struct Params {
   __nv_bfloat16 *out;
   float *lse;
   int32_t *d_err;
+  uint64_t wait_ns;
 };
 
 // ---------------------------------------------------------------------------
@@ -396,6 +400,9 @@ __device__ void producer_role(const Params &P, const CUtensorMap *tmap_q, uint8_
   const int *lists = reinterpret_cast<const int *>(smem + kOffList);
   uint32_t g = 0;  // chunks produced by this CTA
   uint32_t qi = 0;
+  // the Q copy last issued by this thread and not yet seen complete (its
+  // phase parity), or -1: it must land before the CTA exits
+  int tma_pending = -1;
   for (int q = blockIdx.x; q < P.b.num_q; q += gridDim.x, ++qi) {
     // ---- Q of this query: eight 64 x 64 bf16 boxes by TMA, landing in the
     // SW128 layout (heads past n_heads are the map's zero fill); converted to
@@ -406,6 +413,7 @@ __device__ void producer_role(const Params &P, const CUtensorMap *tmap_q, uint8_
 #pragma unroll
       for (int b = 0; b < kDim / 64; ++b)
         tma_load_3d(Qs + b * kQBlock, tmap_q, b * 64, 0, q, &ms->q_tma);
+      tma_pending = (int)(qi & 1);
     }
     // ---- row list and counts of this query (built one query ahead by the
     // first softmax warp)
@@ -439,6 +447,7 @@ __device__ void producer_role(const Params &P, const CUtensorMap *tmap_q, uint8_
     // overlaps the copy and the conversion
     load_step<kFp4>(list, S, row0, 0, b0);
     if (!wait_bar(&ms->q_tma, qi & 1, ms)) break;
+    tma_pending = -1;
     // in batches: every shared-memory read of a batch is issued before its
     // conversions and stores
     constexpr int kQBatch = 4;
@@ -494,6 +503,11 @@ __device__ void producer_role(const Params &P, const CUtensorMap *tmap_q, uint8_
     }
     g += nch;
     if (!ok) break;
+  }
+  if (tma_pending >= 0) {   // an abort left a Q copy in flight: let it land
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(&ms->q_tma, (uint32_t)tma_pending) && globaltimer() - t0 < kWaitNs) {
+    }
   }
 }
 
@@ -841,6 +855,7 @@ attn_tc_kernel(Params P, const __grid_constant__ CUtensorMap tmap_q) {
       mbar_init(&ms->meta_full[i], 1);
     }
     ms->abort = 0;
+    ms->wait_ns = P.wait_ns;
     mbar_fence_init();
   }
   if (warp == kMmaWarp) {
@@ -938,6 +953,7 @@ int attn_tc(const Batch &b, int n_heads, const __nv_bfloat16 *q, const uint8_t *
   P.out = out;
   P.lse = lse;
   P.d_err = d_err;
+  P.wait_ns = wait_limit_ns();
   const int grid = b.num_q < sm_count() ? b.num_q : sm_count();
   CUtensorMap tmap_q;
   if (!make_q_map(&tmap_q, q, n_heads, b.num_q)) return CSA2_ERR_UNSUPPORTED;

@@ -41,6 +41,15 @@ static inline int sm_count() {
   return c;
 }
 
+// Bound on the pipeline waits of the tensor-core kernels (ns of %globaltimer),
+// read when a launch is issued; set by csa2_set_wait_limit_ns.
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+inline std::atomic<uint64_t> &wait_limit_store() {
+  static std::atomic<uint64_t> v{kDefaultWaitNs};
+  return v;
+}
+static inline uint64_t wait_limit_ns() { return wait_limit_store().load(std::memory_order_relaxed); }
+
 // ---------------------------------------------------------------------------
 // batch view on the device (plain copy of the host struct's pointers)
 // ---------------------------------------------------------------------------

@@ -30,7 +30,9 @@
 // Prologue: the query operand's loads are issued first, the tile geometry is
 // worked out while they are in flight, and the producers start on the key
 // tiles while warps 0-8 dequantise the query operand and allocate TMEM.
-// Waits are time-bounded (CSA2_DERR_TIMEOUT on expiry).
+// Waits are time-bounded (two seconds unless csa2_set_wait_limit_ns says
+// otherwise; CSA2_DERR_TIMEOUT on expiry, after which the MMAs in flight are
+// drained for at most two seconds and TMEM is freed).
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tcgen05.cuh"
@@ -62,7 +64,7 @@ constexpr uint32_t kOffCand = kOffMisc + 4096;         // candidate blocks of th
 constexpr int kCandInts = 4096;                        // (16 KB; used when they fit)
 constexpr uint32_t kSmemBytes = kOffCand + kCandInts * 4;
 
-constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kWaitNs = 2000000000ull;   // the MMA drain (pipeline waits: Params::wait_ns)
 constexpr int kDerrTimeout = 128;
 constexpr int kMaxQT = 32;
 
@@ -76,6 +78,7 @@ struct RunInfo {
 
 struct Misc {
   uint64_t a_full[kStages], a_empty[kStages], d_full[2], d_empty[2], done;
+  uint64_t wait_ns;          // bound on every pipeline wait
   uint32_t tmem_base;
   int abort;
   int nruns;
@@ -103,7 +106,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Misc *m
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
     if (*(volatile int *)&ms->abort) return false;
-    if (globaltimer() - t0 > kWaitNs) {
+    if (globaltimer() - t0 > ms->wait_ns) {
       atomicExch(&ms->abort, 1);
       return false;
     }
@@ -151,6 +154,7 @@ struct Params {
   float *scores;
   int64_t ld;
   int32_t *d_err;
+  uint64_t wait_ns;
 };
 
 // Candidate-block view of the tile, copied to registers once per tile: block
@@ -484,6 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
   }
   if (threadIdx.x == 0) {
     ms->abort = 0;
+    ms->wait_ns = P.wait_ns;
     ms->cand_smem = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&ms->a_full[i], kProdWarps);
@@ -661,6 +666,7 @@ int index_score_tc(const Batch &b, int n_heads, const uint8_t *q_fp4, const floa
   P.scores = scores;
   P.ld = ld;
   P.d_err = d_err;
+  P.wait_ns = wait_limit_ns();
   int64_t max_len = cand_blocks ? (int64_t)max_blocks * block : ld;
   if (max_len > ld) max_len = ld;
   const int64_t chunks = (max_len + kKeyTile * kTilesPerChunk - 1) / (kKeyTile * kTilesPerChunk);

@@ -116,6 +116,45 @@ __device__ __forceinline__ void mma_f16_split(uint32_t d_tmem, uint32_t a_lo, ui
       : "memory");
 }
 
+// kind::f8f6f4 without block scaling: 8-bit operands (the formats are in the
+// instruction descriptor; E4M3 is code 0, so make_idesc_f16's bits describe
+// E4M3 x E4M3 -> f32), K = 32 per instruction (32 bytes of a K-major row).
+__device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of the block-scaled kind::mxf4: E2M1 x E2M1 -> f32,
+// UE8M0 scales, K-major operands, K = 64 per instruction.
+//   [4,6) B scale-factor id   [7,10) A format (E2M1 = 1)   [10,13) B format
+//   [17,23) N >> 3   [23] scale format (1 = UE8M0)   [24,29) M >> 4
+//   [29,31) A scale-factor id   [31] K size (0: K = 64)
+__host__ __device__ constexpr uint32_t make_idesc_mxf4(uint32_t m, uint32_t n, uint32_t a_sf_id,
+                                                       uint32_t b_sf_id) {
+  return ((b_sf_id & 3u) << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | (1u << 23) |
+         ((m >> 4) << 24) | ((a_sf_id & 3u) << 29);
+}
+
+// kind::mxf4 with one UE8M0 scale per 32 elements (scale_vec::2X): packed
+// E2M1 operands (two per byte, 32 bytes of a K-major row per instruction);
+// the scale factors of A and B are read from TMEM at sfa / sfb.
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t *mbar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(

@@ -57,13 +57,23 @@ class LayerRunner:
         self.nblocks = torch.empty(nq, dtype=torch.int32, device=dev)
         self.tail = None
         self.batches = {name: w.batch(name, rows) for name in w.layers}
+        # per-layer per-row tensors restricted to the runner's rows, gathered
+        # once here so that the call sequences launch only the library's kernels
+        self._rows_t = {}
+        if rows is not None:
+            for name, L in w.layers.items():
+                for attr in ("q", "q_fp4", "q_scale", "head_w", "win_lo", "given_idx"):
+                    t = getattr(L, attr, None)
+                    if t is not None:
+                        self._rows_t[(name, attr)] = t[rows].contiguous()
 
     # ---- per-layer tensors restricted to the runner's rows -------------------
     def _lt(self, layer: str, attr: str):
         t = getattr(self.w.layers[layer], attr)
         if t is None or self.rows is None:
             return t
-        return t[self.rows].contiguous()
+        got = self._rows_t.get((layer, attr))
+        return got if got is not None else t[self.rows].contiguous()
 
     # ---- a1 -------------------------------------------------------------------
     def tail_layout(self):
@@ -150,10 +160,23 @@ class LayerRunner:
         return self.out[layer], self.lse[layer]
 
     # ---- whole layers -------------------------------------------------------------
-    def full_layer(self, layer: str):
-        s = self.score_full(layer)
-        idx, _ = self.select(layer, s)
-        return self.attend(layer, idx)
+    def full_layer(self, layer: str, events=None):
+        """Score, select and attend.  When `events` is a dict, each launch is
+        bracketed by CUDA events on the current stream, appended under
+        "score", "select" and "attend"."""
+        def timed(kind, fn):
+            if events is None:
+                return fn()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            r = fn()
+            e1.record()
+            events.setdefault(kind, []).append((e0, e1))
+            return r
+        s = timed("score", lambda: self.score_full(layer))
+        idx, _ = timed("select", lambda: self.select(layer, s))
+        return timed("attend", lambda: self.attend(layer, idx))
 
     def source_layer(self, layer: str, win_lo=None, events=None):
         s = self.score_full(layer)
