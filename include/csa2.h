@@ -94,7 +94,7 @@ typedef struct CUstream_st *csa2_stream_t; /* same object as cudaStream_t */
  *   ratio       m in {1, 2}: each compressed entry covers m consecutive tokens
  *               without overlap, so entry j is visible to position t once its
  *               last token m*j+m-1 <= t: n_vis(t) = floor((t+1)/m)
- *               ([CSA2] "压缩器也改了"; [D0] sec. 1). */
+ *               ([CSA2] CSA2 card, paragraph on the compressor; [D0] sec. 1). */
 typedef struct csa2_batch {
   int32_t num_q;
   int32_t num_req;
@@ -152,7 +152,8 @@ CSA2_API int csa2_tail_layout(int32_t num_req, const int32_t *extend_len,
 
 /* ---------------------------------------------------------------------------
  * a2-a4, a7. Index scores   [CSA2] CSA2 and Hierarchical cards; [D0] sec. 2
- * and sec. 5 ("FP4 索引与 TP 布局": MQA-shaped, heads replicated).
+ * and sec. 5, on the FP4 indexer and its TP layout: MQA-shaped, heads
+ * replicated.
  *
  *   s(q, j) = sum_h w[q,h] * max(0, sum_d Qi[q,h,d] * Ki[j,d])
  *
@@ -199,7 +200,8 @@ CSA2_API int csa2_topk(const csa2_batch *b, const float *scores, int64_t ld, int
 
 /* ---------------------------------------------------------------------------
  * a5, a6. Top-K plus hierarchical candidate blocks (L20-style source)
- * [CSA2] Hierarchical card ("按 8 个一组归为 block ... 最多 2,048 个 block");
+ * [CSA2] Hierarchical card (entries grouped into blocks of 8, at most 2048
+ * blocks kept);
  * [D0] sec. 2 (latest block always kept; no exclusion when everything fits).
  *
  * From full-visible scores (as csa2_index_score with cand_blocks == NULL):
@@ -219,6 +221,38 @@ CSA2_API int csa2_topk_candidates(const csa2_batch *b, const float *scores, int6
                          int32_t *idx, int32_t *count, int32_t *blocks,
                          int32_t *nblocks, int32_t *d_err,
                          csa2_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * a3 + a5 streamed (NEXT-4a). Index score and top-K in one pass over the keys
+ * [CSA2] Hierarchical card (the block-max, candidate and Top-K data movement
+ * is a cost of its own); [D0] sec. 2 and 5.
+ *
+ * For full-visible rows (Full and Reindex layers scoring every visible
+ * entry): the same selection as csa2_index_score (cand_blocks == NULL, ld =
+ * max_len) followed by csa2_topk, without writing score rows.  A sample pass
+ * scores every 8th key tile of 128 keys and sets a per-query threshold; the
+ * scoring pass then appends only the (entry, score) pairs at or above it to
+ * a per-query list (at most 4096 pairs); the selection is exact on any list
+ * that holds at least k of them (rows of at most 4096 visible entries list
+ * everything).  Rows whose list misses are rescored on the CUDA cores with
+ * the scoring's own arithmetic, so the result is exact either way.
+ *   max_len   bound on every row's visible entries (rows longer are cut,
+ *             CSA2_DERR_LD, as with ld in csa2_index_score)
+ *   idx/count as csa2_topk
+ *   workspace device scratch of at least csa2_index_topk_workspace(num_q,
+ *             max_len) bytes, 256-byte aligned, owned by the caller; its
+ *             contents on entry do not matter and are undefined after the
+ *             call.  Calls sharing one workspace must not overlap.
+ * Operand layouts, flags and support as csa2_index_score; 1 <= k <= 2048.
+ * ------------------------------------------------------------------------- */
+CSA2_API int csa2_index_topk_workspace(int32_t num_q, int64_t max_len, int64_t *bytes);
+CSA2_API int csa2_index_topk(const csa2_batch *b, int32_t n_heads, int32_t head_dim,
+                             const uint8_t *q_fp4, const float *q_scale,
+                             const float *head_w, const uint8_t *k_fp4,
+                             const float *k_scale, int64_t max_len, int32_t k,
+                             int32_t *idx, int32_t *count, void *workspace,
+                             int64_t workspace_bytes, int32_t *d_err,
+                             csa2_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * a8-a10. Sparse + sliding-window attention under one softmax
@@ -255,9 +289,9 @@ CSA2_API int csa2_sparse_swa_attn(const csa2_batch *b, int32_t n_heads, int32_t 
                          int32_t *d_err, csa2_stream_t stream);
 
 /* ---------------------------------------------------------------------------
- * a10 with the FP4 main-KV layout  [CSA2] mixed-precision card ("Main KV:
- * E2M1 数据；每 16 通道一个 E4M3 scale；省略 NVFP4 的二级全局 scale";
- * 512 x (0.5 + 1/16) = 288 B per entry; SWA stays FP8).
+ * a10 with the FP4 main-KV layout  [CSA2] mixed-precision card (main KV as
+ * E2M1 data with one E4M3 scale per 16 channels and no second-level global
+ * scale: 512 x (0.5 + 1/16) = 288 B per entry; SWA stays FP8).
  *
  * The same attention as csa2_sparse_swa_attn, with the selected rows read from
  * an FP4 pool:
@@ -278,8 +312,9 @@ CSA2_API int csa2_sparse_swa_attn_fp4kv(const csa2_batch *b, int32_t n_heads, in
 
 /* ---------------------------------------------------------------------------
  * Encoder-side bounded replay layout   [CSA2] Encoder Bounded Replay card
- * ("只重放已缓存前缀的最近 128 token，再继续处理新后缀"; replayed tokens only
- * regenerate SWA KV and never overwrite the cached global KV); [D0] sec. 4.1
+ * (on a prefix hit the last 128 cached tokens are processed again before the
+ * new suffix; replayed tokens only regenerate SWA KV and never overwrite the
+ * cached global KV); [D0] sec. 4.1
  * and 4.3 (local attention is cut at the rebuild boundary).
  *
  * For each request r with P_r = prefix_len[r] cached tokens (global entries
@@ -339,9 +374,10 @@ CSA2_API int csa2_rows_scatter(const int32_t *count, int64_t capacity,
 
 /* ---------------------------------------------------------------------------
  * Quantise-and-write of cache rows   [CSA2] mixed-precision card (main KV FP8
- * block-32 or "E2M1 数据；每 16 通道一个 E4M3 scale", index K MXFP4 per 32);
- * [D0] sec. 5 ("保持量化语义的融合": fusing the quantise, pack and cache write
- * must keep the intermediate rounding and scaling).
+ * block-32, or E2M1 with one E4M3 scale per 16 channels; index K MXFP4 per
+ * 32); [D0] sec. 5, on fusions that keep the quantisation semantics: fusing
+ * the quantise, pack and cache write must keep the intermediate rounding and
+ * scaling.
  *
  * Row i of src ([n, dim] fp32, 16-byte aligned) is quantised into row
  * dst_row[i] of a cache of `rows` rows.  Per group of G channels with

@@ -29,7 +29,8 @@ FMT_FP8_B32, FMT_FP4KV, FMT_MXFP4 = 1, 2, 3
 EXPORTED = ("csa2_status_string", "csa2_tail_layout", "csa2_index_score", "csa2_topk",
             "csa2_topk_candidates", "csa2_sparse_swa_attn", "csa2_sparse_swa_attn_fp4kv",
             "csa2_encoder_replay_layout", "csa2_rows_gather", "csa2_rows_scatter",
-            "csa2_quantize_rows", "csa2_set_wait_limit_ns")
+            "csa2_quantize_rows", "csa2_set_wait_limit_ns", "csa2_index_topk_workspace",
+            "csa2_index_topk")
 
 
 class Csa2Error(RuntimeError):
@@ -74,10 +75,31 @@ def load(path: Optional[str] = None):
     lib.csa2_rows_scatter.argtypes = [vp, i64, vp, vp, vp, i64, i64, vp, vp]
     lib.csa2_quantize_rows.argtypes = [i32, i64, vp, i32, vp, vp, vp, i64, vp, vp]
     lib.csa2_set_wait_limit_ns.argtypes = [C.c_uint64]
+    lib.csa2_index_topk_workspace.argtypes = [i32, i64, vp]
+    lib.csa2_index_topk.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, i64, i32, vp, vp, vp, i64,
+                                    vp, vp]
     for name in EXPORTED[1:]:
         getattr(lib, name).restype = C.c_int
     _lib = lib
     return lib
+
+
+def csa2_index_topk_workspace(num_q, max_len) -> int:
+    """Workspace bytes csa2_index_topk needs for num_q rows of at most max_len
+    visible entries."""
+    out = C.c_int64(0)
+    _check(load().csa2_index_topk_workspace(int(num_q), int(max_len), C.byref(out)),
+           "csa2_index_topk_workspace")
+    return int(out.value)
+
+
+def csa2_index_topk(batch, n_heads, head_dim, q_fp4, q_scale, head_w, k_fp4, k_scale, max_len,
+                    k, idx, count, workspace, workspace_bytes, d_err, stream=None) -> int:
+    st, keep = make_batch(batch)
+    return load().csa2_index_topk(C.byref(st), int(n_heads), int(head_dim), _ptr(q_fp4),
+                                  _ptr(q_scale), _ptr(head_w), _ptr(k_fp4), _ptr(k_scale),
+                                  int(max_len), int(k), _ptr(idx), _ptr(count), _ptr(workspace),
+                                  int(workspace_bytes), _ptr(d_err), _stream(stream))
 
 
 def csa2_set_wait_limit_ns(ns: int) -> int:
@@ -321,6 +343,27 @@ def topk_candidates(batch, scores, k=512, block=8, max_blocks=2048, d_err=None, 
     _check(csa2_topk_candidates(batch, scores, scores.shape[1], k, block, max_blocks, idx, count,
                                 blocks, nblocks, d_err, stream), "csa2_topk_candidates")
     return idx, count, blocks, nblocks
+
+
+def index_topk(batch, q_fp4, q_scale, head_w, k_fp4, k_scale, max_len, k, idx=None,
+               count=None, workspace=None, d_err=None, stream=None):
+    """Top-k entries of every query by index score, scored and selected in one
+    streamed pass (no score rows).  Allocates the outputs and, if not given,
+    the workspace (uint8, csa2_index_topk_workspace bytes)."""
+    nq = int(batch["num_q"])
+    dev = q_fp4.device
+    if idx is None:
+        idx = torch.empty((nq, int(k)), dtype=torch.int32, device=dev)
+    if count is None:
+        count = torch.empty(nq, dtype=torch.int32, device=dev)
+    need = csa2_index_topk_workspace(nq, max_len)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _check(csa2_index_topk(batch, q_fp4.shape[1], q_fp4.shape[2] * 2, q_fp4, q_scale, head_w,
+                           k_fp4, k_scale, max_len, k, idx, count, workspace,
+                           workspace.numel() * workspace.element_size(), d_err, stream),
+           "csa2_index_topk")
+    return idx, count
 
 
 def sparse_swa_attn(batch, q, kv_fp8, kv_scale, idx, swa_fp8, swa_scale, win_lo=None, window=128,

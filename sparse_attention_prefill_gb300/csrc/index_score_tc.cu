@@ -91,6 +91,8 @@ struct Misc {
   int ident[kMaxQT];         // pool mode: blocks are 0..nb-1
   int cand_smem;             // pool mode: the chunk's candidate blocks are in shared memory
   int cand_span, b_lo;       //   as [query of the tile][block - b_lo]
+  int stride;                // key tiles: every stride-th tile (sample mode), else 1
+  float thr[kMaxQT];         // list mode: per-query threshold
   alignas(16) float w[256];  // head weights of the tile, halved
 };
 static_assert(sizeof(Misc) <= 4096, "misc");
@@ -152,10 +154,26 @@ struct Params {
   const int32_t *cand;
   int block, max_blocks;
   float *scores;
-  int64_t ld;
+  int64_t ld;          // row capacity in entries (rows past it are cut, CSA2_DERR_LD)
+  int64_t out_ld;      // row stride of `scores` (sample mode: ld / stride tiles)
+  int stride;          // 1: every key tile; S: tiles 0, S, 2S, .. only, stored densely
+  // list mode (list_cnt != nullptr): no dense scores; each query appends the
+  // (entry, score) pairs with score >= list_thr[q] to its list of list_cap
+  // slots (the counter keeps counting past the capacity)
+  const float *list_thr;
+  uint32_t *list_cnt;
+  int32_t *list_ent;
+  float *list_val;
+  int list_cap;
   int32_t *d_err;
   uint64_t wait_ns;
 };
+
+// key tiles of a row of `len` keys walked by this launch (every stride-th)
+__device__ __forceinline__ int64_t walked_tiles(int64_t len, int stride) {
+  const int64_t nt = (len + kKeyTile - 1) / kKeyTile;
+  return (nt + stride - 1) / stride;
+}
 
 // Candidate-block view of the tile, copied to registers once per tile: block
 // of slot s (a shift for power-of-two block sizes), and the entry it holds.
@@ -205,7 +223,7 @@ static_assert(kProdThreads % 4 == 0, "a thread's items share one 32-dim group");
 __device__ __forceinline__ void load_tile(const Params &P, const Misc *ms, const CandView &cv,
                                           int ri, int64_t kt, int q0, int ptid, KeyLoad &L) {
   const RunInfo ru = ms->runs[ri];
-  const int s0 = (int)kt * kKeyTile;
+  const int s0 = (int)kt * ms->stride * kKeyTile;
   const int lim = (int)(ru.gather ? ru.len : min(ru.len, ru.lim));
   const int64_t nvis = ms->n_vis[ru.ql0];
   L.valid = 0;
@@ -231,7 +249,7 @@ __device__ __forceinline__ void load_tile(const Params &P, const Misc *ms, const
 __device__ __forceinline__ bool next_item(const Misc *ms, int y, int &ri, int64_t &kt) {
   ++kt;
   while (ri < ms->nruns) {
-    const int64_t nt = (ms->runs[ri].len + kKeyTile - 1) / kKeyTile;
+    const int64_t nt = walked_tiles(ms->runs[ri].len, ms->stride);
     const int64_t hi = min(nt, (int64_t)(y + 1) * kTilesPerChunk);
     if (kt < hi) return true;
     ++ri;
@@ -309,7 +327,7 @@ __device__ void mma_role(const Params &P, uint8_t *smem, Misc *ms, int y) {
     bool ok = true;
     for (int ri = 0; ri < ms->nruns && ok; ++ri) {
       const RunInfo ru = ms->runs[ri];
-      const int64_t nt = (ru.len + kKeyTile - 1) / kKeyTile;
+      const int64_t nt = walked_tiles(ru.len, ms->stride);
       uint32_t n = (uint32_t)(ru.nq * P.hi);
       n = (n + 15u) & ~15u;
       const uint32_t idesc = make_idesc_f16(128, n, false, false);
@@ -353,22 +371,40 @@ __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
   bool ok = true;
   for (int ri = 0; ri < ms->nruns && ok; ++ri) {
     const RunInfo ru = ms->runs[ri];
-    const int64_t nt = (ru.len + kKeyTile - 1) / kKeyTile;
+    const int64_t nt = walked_tiles(ru.len, ms->stride);
     for (int64_t kt = (int64_t)y * kTilesPerChunk;
          kt < nt && kt < (int64_t)(y + 1) * kTilesPerChunk; ++kt, ++it) {
       const uint32_t db = it & 1;
       if (!(ok = wait_bar(&ms->d_full[db], (it >> 1) & 1, ms))) break;
       fence_after_sync();
-      const int s = (int)kt * kKeyTile + 32 * sp + lane;
-      // w . ReLU(D) over the HI head columns of query ql; store
+      const int r = 32 * sp + lane;                       // key of the tile
+      const int s = (int)kt * ms->stride * kKeyTile + r;  // its slot in the row
+      const int col = (int)kt * kKeyTile + r;             // its column in `scores`
+      // w . ReLU(D) over the HI head columns of query ql; store, or append to
+      // the query's list (called by the whole warp: the append is
+      // warp-aggregated, one counter update per warp)
       auto finish = [&](int ql, float acc) {
-        if (s < ms->row_len[ql]) {
-          float outv = acc;
-          if (P.cand) {
-            const int64_t j = ru.gather ? cv.entry(ql, q0 + ql, s) : s;
-            if (j >= ms->n_vis[ql]) outv = -INFINITY;
-          }
-          P.scores[(int64_t)(q0 + ql) * P.ld + s] = outv;
+        const bool in = s < ms->row_len[ql];
+        float outv = acc;
+        if (in && P.cand) {
+          const int64_t j = ru.gather ? cv.entry(ql, q0 + ql, s) : s;
+          if (j >= ms->n_vis[ql]) outv = -INFINITY;
+        }
+        if (P.list_cnt == nullptr) {
+          if (in) P.scores[(int64_t)(q0 + ql) * P.out_ld + col] = outv;
+          return;
+        }
+        const bool take = in && outv >= ms->thr[ql];
+        const uint32_t m = __ballot_sync(0xffffffffu, take);
+        if (m == 0u) return;
+        const int leader = __ffs(m) - 1;
+        uint32_t base = 0;
+        if (lane == leader) base = atomicAdd(P.list_cnt + q0 + ql, (uint32_t)__popc(m));
+        base = __shfl_sync(0xffffffffu, base, leader) + __popc(m & ((1u << lane) - 1u));
+        if (take && base < (uint32_t)P.list_cap) {
+          const int64_t o = (int64_t)(q0 + ql) * P.list_cap + base;
+          P.list_ent[o] = s;
+          P.list_val[o] = outv;
         }
       };
       // w * ReLU(x) as (w/2) * (x + |x|): the same value (halving and
@@ -486,8 +522,12 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
     ms->row_len[threadIdx.x] = 0;
     ms->n_vis[threadIdx.x] = 0;
   }
+  if (threadIdx.x < QT)
+    ms->thr[threadIdx.x] = (P.list_thr && q0 + (int)threadIdx.x < P.b.num_q)
+                               ? P.list_thr[q0 + threadIdx.x] : 0.f;
   if (threadIdx.x == 0) {
     ms->abort = 0;
+    ms->stride = P.stride;
     ms->wait_ns = P.wait_ns;
     ms->cand_smem = 0;
     for (int i = 0; i < kStages; ++i) {
@@ -584,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
   // does this CTA's key chunk hold any work?
   bool any = false;
   for (int ri = 0; ri < ms->nruns; ++ri)
-    any |= (ms->runs[ri].len + kKeyTile - 1) / kKeyTile > (int64_t)y * kTilesPerChunk;
+    any |= walked_tiles(ms->runs[ri].len, ms->stride) > (int64_t)y * kTilesPerChunk;
   if (!any) {
     raise_err(P.d_err, err);
     return;
@@ -644,35 +684,17 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
 
 }  // namespace
 
-int index_score_tc(const Batch &b, int n_heads, const uint8_t *q_fp4, const float *q_scale,
-                   const float *head_w, const uint8_t *k_fp4, const float *k_scale,
-                   const int32_t *cand_blocks, int block, int max_blocks, float *scores,
-                   int64_t ld, int32_t *d_err, cudaStream_t st) {
-  if (b.num_q == 0) return CSA2_OK;
-  if (((uintptr_t)q_fp4 | (uintptr_t)k_fp4) & 15u) return CSA2_ERR_UNSUPPORTED;
-  if (((uintptr_t)q_scale | (uintptr_t)k_scale) & 15u) return CSA2_ERR_UNSUPPORTED;
-  Params P;
-  P.b = b;
-  P.hi = n_heads;
-  P.qt = 256 / n_heads;
-  P.q_fp4 = q_fp4;
-  P.q_scale = q_scale;
-  P.head_w = head_w;
-  P.k_fp4 = k_fp4;
-  P.k_scale = k_scale;
-  P.cand = cand_blocks;
-  P.block = block;
-  P.max_blocks = max_blocks;
-  P.scores = scores;
-  P.ld = ld;
-  P.d_err = d_err;
+namespace {
+
+int launch(Params &P, int n_heads, cudaStream_t st) {
   P.wait_ns = wait_limit_ns();
-  int64_t max_len = cand_blocks ? (int64_t)max_blocks * block : ld;
-  if (max_len > ld) max_len = ld;
-  const int64_t chunks = (max_len + kKeyTile * kTilesPerChunk - 1) / (kKeyTile * kTilesPerChunk);
+  int64_t max_len = P.cand ? (int64_t)P.max_blocks * P.block : P.ld;
+  if (max_len > P.ld) max_len = P.ld;
+  const int64_t tiles_walked = (((max_len + kKeyTile - 1) / kKeyTile) + P.stride - 1) / P.stride;
+  const int64_t chunks = (tiles_walked + kTilesPerChunk - 1) / kTilesPerChunk;
   if (chunks == 0) return CSA2_OK;
   if (chunks > 65535) return CSA2_ERR_UNSUPPORTED;
-  const int64_t tiles = (b.num_q + P.qt - 1) / P.qt;
+  const int64_t tiles = (P.b.num_q + P.qt - 1) / P.qt;
   dim3 grid((unsigned)tiles, (unsigned)chunks);
 #define CSA2_LAUNCH(H)                                                                     \
   do {                                                                                     \
@@ -689,6 +711,77 @@ int index_score_tc(const Batch &b, int n_heads, const uint8_t *q_fp4, const floa
   }
 #undef CSA2_LAUNCH
   return launch_status();
+}
+
+bool base_params(Params &P, const Batch &b, int n_heads, const uint8_t *q_fp4,
+                 const float *q_scale, const float *head_w, const uint8_t *k_fp4,
+                 const float *k_scale, int64_t ld, int32_t *d_err) {
+  if (((uintptr_t)q_fp4 | (uintptr_t)k_fp4) & 15u) return false;
+  if (((uintptr_t)q_scale | (uintptr_t)k_scale) & 15u) return false;
+  P = Params{};
+  P.b = b;
+  P.hi = n_heads;
+  P.qt = 256 / n_heads;
+  P.q_fp4 = q_fp4;
+  P.q_scale = q_scale;
+  P.head_w = head_w;
+  P.k_fp4 = k_fp4;
+  P.k_scale = k_scale;
+  P.cand = nullptr;
+  P.block = 1;
+  P.max_blocks = 1;
+  P.ld = ld;
+  P.out_ld = ld;
+  P.stride = 1;
+  P.d_err = d_err;
+  return true;
+}
+
+}  // namespace
+
+int index_score_tc(const Batch &b, int n_heads, const uint8_t *q_fp4, const float *q_scale,
+                   const float *head_w, const uint8_t *k_fp4, const float *k_scale,
+                   const int32_t *cand_blocks, int block, int max_blocks, float *scores,
+                   int64_t ld, int32_t *d_err, cudaStream_t st) {
+  if (b.num_q == 0) return CSA2_OK;
+  Params P;
+  if (!base_params(P, b, n_heads, q_fp4, q_scale, head_w, k_fp4, k_scale, ld, d_err))
+    return CSA2_ERR_UNSUPPORTED;
+  P.cand = cand_blocks;
+  P.block = block;
+  P.max_blocks = max_blocks;
+  P.scores = scores;
+  return launch(P, n_heads, st);
+}
+
+int index_score_sample(const Batch &b, int n_heads, const uint8_t *q_fp4, const float *q_scale,
+                       const float *head_w, const uint8_t *k_fp4, const float *k_scale,
+                       int64_t max_len, int stride, float *sample, int64_t sample_ld,
+                       int32_t *d_err, cudaStream_t st) {
+  if (b.num_q == 0) return CSA2_OK;
+  Params P;
+  if (!base_params(P, b, n_heads, q_fp4, q_scale, head_w, k_fp4, k_scale, max_len, d_err))
+    return CSA2_ERR_UNSUPPORTED;
+  P.stride = stride;
+  P.scores = sample;
+  P.out_ld = sample_ld;
+  return launch(P, n_heads, st);
+}
+
+int index_score_list(const Batch &b, int n_heads, const uint8_t *q_fp4, const float *q_scale,
+                     const float *head_w, const uint8_t *k_fp4, const float *k_scale,
+                     int64_t max_len, const float *thr, uint32_t *cnt, int32_t *ent, float *val,
+                     int cap, int32_t *d_err, cudaStream_t st) {
+  if (b.num_q == 0) return CSA2_OK;
+  Params P;
+  if (!base_params(P, b, n_heads, q_fp4, q_scale, head_w, k_fp4, k_scale, max_len, d_err))
+    return CSA2_ERR_UNSUPPORTED;
+  P.list_thr = thr;
+  P.list_cnt = cnt;
+  P.list_ent = ent;
+  P.list_val = val;
+  P.list_cap = cap;
+  return launch(P, n_heads, st);
 }
 
 }  // namespace csa2

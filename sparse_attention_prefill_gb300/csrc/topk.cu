@@ -550,6 +550,59 @@ __device__ void row_geometry(const Batch &b, int q, const int32_t *cand_blocks, 
 
 // minimum residency chosen so the key registers do not spill
 
+// Exact top k of the n listed (key, position) pairs in sh.list_key /
+// sh.list_pos, given bounds mn <= key <= mx on every listed key and at least
+// k listed keys: the k-th key by radix, and the keys equal to it, if only
+// some are taken, by a second radix over their inverted positions (lowest
+// positions first).  emit(i, slot) gets the list index i of every selected
+// pair, with distinct slots 0..k-1.
+template <int NT, class Emit>
+__device__ void select_listed(int n_list, uint32_t mn, uint32_t mx, uint32_t k,
+                              RegShared<NT> &sh, Emit emit) {
+  const int t = threadIdx.x;
+  if (t == 0) sh.out_count = 0;
+  __syncthreads();
+  uint32_t prefix, rem;
+  bool whole;
+  radix_kth<NT>(
+      [&](auto f) {
+        for (int i = t; i < n_list; i += NT) f(sh.list_key[i]);
+      },
+      mn, mx, k, sh, prefix, rem, whole);
+  const uint32_t lo = whole ? prefix : prefix + 1u;
+  for (int i0 = 0; i0 < n_list; i0 += NT) {
+    const int i = i0 + t;
+    const uint32_t x = i < n_list ? sh.list_key[i] : 0u;
+    const bool take = x != 0u && x >= lo;
+    const uint32_t slot = warp_reserve(take, &sh.out_count);
+    if (take) emit(i, slot);
+  }
+  if (!whole) {
+    // the rem lowest positions among the listed keys equal to prefix:
+    // largest inverted positions (positions are below 2^31, so these keys are
+    // nonzero and distinct)
+    auto inv = [&](int i) -> uint32_t {
+      return sh.list_key[i] == prefix ? 0xffffffffu - (uint32_t)sh.list_pos[i] : 0u;
+    };
+    uint32_t p2, rem2;
+    bool whole2;
+    radix_kth<NT>(
+        [&](auto f) {
+          for (int i = t; i < n_list; i += NT) f(inv(i));
+        },
+        0x80000000u, 0xffffffffu, rem, sh, p2, rem2, whole2);
+    const uint32_t lo2 = whole2 ? p2 : p2 + 1u;
+    for (int i0 = 0; i0 < n_list; i0 += NT) {
+      const int i = i0 + t;
+      const uint32_t y = i < n_list ? inv(i) : 0u;
+      const bool take = y != 0u && (y >= lo2 || (!whole2 && y == p2));
+      const uint32_t slot = warp_reserve(take, &sh.out_count);
+      if (take) emit(i, slot);
+    }
+  }
+  __syncthreads();
+}
+
 // Long rows (past the register path): a threshold guess from the moments of
 // every 16th key, then one sweep that lists the keys at or above it (up to
 // kListCap, with their positions).  With between k and kListCap keys listed
@@ -636,45 +689,8 @@ __device__ bool select_topk_listed(const Keys &keys, int64_t n, uint32_t k, RegS
   if (t == 0) sh.out_count = 0;
   __syncthreads();
   if (n_list < k || n_list > (uint32_t)kListCap) return false;
-  uint32_t prefix, rem;
-  bool whole;
-  radix_kth<NT>(
-      [&](auto f) {
-        for (int i = t; i < (int)n_list; i += NT) f(sh.list_key[i]);
-      },
-      t_est, mx, k, sh, prefix, rem, whole);
-  const uint32_t lo = whole ? prefix : prefix + 1u;
-  for (int i0 = 0; i0 < (int)n_list; i0 += NT) {
-    const int i = i0 + t;
-    const uint32_t x = i < (int)n_list ? sh.list_key[i] : 0u;
-    const bool take = x != 0u && x >= lo;
-    const uint32_t slot = warp_reserve(take, &sh.out_count);
-    if (take) emit(sh.list_pos[i], slot);
-  }
-  if (!whole) {
-    // the rem lowest positions among the listed keys equal to prefix:
-    // largest inverted positions (positions are below 2^31, so these keys are
-    // nonzero and distinct)
-    auto inv = [&](int i) -> uint32_t {
-      return sh.list_key[i] == prefix ? 0xffffffffu - (uint32_t)sh.list_pos[i] : 0u;
-    };
-    uint32_t p2, rem2;
-    bool whole2;
-    radix_kth<NT>(
-        [&](auto f) {
-          for (int i = t; i < (int)n_list; i += NT) f(inv(i));
-        },
-        0x80000000u, 0xffffffffu, rem, sh, p2, rem2, whole2);
-    const uint32_t lo2 = whole2 ? p2 : p2 + 1u;
-    for (int i0 = 0; i0 < (int)n_list; i0 += NT) {
-      const int i = i0 + t;
-      const uint32_t y = i < (int)n_list ? inv(i) : 0u;
-      const bool take = y != 0u && (y >= lo2 || (!whole2 && y == p2));
-      const uint32_t slot = warp_reserve(take, &sh.out_count);
-      if (take) emit(sh.list_pos[i], slot);
-    }
-  }
-  __syncthreads();
+  select_listed<NT>((int)n_list, t_est, mx, k, sh,
+                    [&](int i, uint32_t slot) { emit(sh.list_pos[i], slot); });
   return true;
 }
 
@@ -802,6 +818,302 @@ candidate_blocks_kernel(Batch b, const float *__restrict__ scores, int64_t ld, i
   if (threadIdx.x == 0) nblocks[q] = max_blocks;
 }
 
+// ---------------------------------------------------------------------------
+// Index score streamed into the top-K (full-visible rows): the scoring pass
+// appends only the (entry, score) pairs at or above a per-query threshold to
+// a bounded list, and the selection runs on that list.
+//  1. sample pass (index score over every kStreamStride-th key tile)
+//  2. stream_threshold_kernel: per query, the score a normal row with the
+//     sample's mean and deviation would have `target` scores above; rows of at
+//     most kStreamCap visible entries list everything (threshold -inf)
+//  3. list pass (index score, appending epilogue)
+//  4. stream_select_kernel: exact top k of the list when it holds every entry
+//     at or above the threshold and at least k of them (or every visible
+//     entry); any other row (a missed guess) is queued for
+//  5. stream_fallback_kernel: the row rescored on the CUDA cores in blocks,
+//     with the scoring epilogue's arithmetic, and an exact running top k.
+// Exactness: a list holding every entry with score >= thr, with at least k of
+// them, holds the k best entries and every entry tied with the k-th (all
+// have score >= the k-th score >= thr); ties are broken by lowest entry.
+// ---------------------------------------------------------------------------
+constexpr int kStreamCap = kStreamListCap;
+static_assert(kStreamCap <= kListCap, "a query's list fits the selection's shared arrays");
+
+__device__ __forceinline__ int64_t stream_nvis(const Batch &b, int q, int64_t max_len) {
+  int64_t nv = n_visible(b.q_pos[q], b.ratio);
+  const int64_t kvl = b.kv_len[b.q_req[q]];
+  if (nv > kvl) nv = kvl;
+  return nv < max_len ? nv : max_len;
+}
+
+// One warp per query.  Also clears the list counters and the fallback queue.
+__global__ void __launch_bounds__(256)
+stream_threshold_kernel(Batch b, int64_t max_len, int k, int stride, StreamWs ws) {
+  if (blockIdx.x == 0 && threadIdx.x < 2) ws.hdr[threadIdx.x] = 0u;
+  const int lane = threadIdx.x & 31;
+  const int q = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (q >= b.num_q) return;
+  const int64_t nv = stream_nvis(b, q, max_len);
+  float thr = -INFINITY;
+  if (nv > kStreamCap) {
+    const int64_t walked = ((nv + 127) / 128 + stride - 1) / stride;
+    const float *row = ws.sample + (int64_t)q * ws.sample_ld;
+    float n = 0.f, sum = 0.f, sq = 0.f;
+    for (int64_t c = lane; c < walked * 128; c += 32) {
+      const int64_t s = (c >> 7) * stride * 128 + (c & 127);
+      if (s < nv) {
+        const float v = row[c];
+        if (fabsf(v) <= 3.0e38f) {
+          n += 1.f;
+          sum += v;
+          sq += v * v;
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      n += __shfl_xor_sync(0xffffffffu, n, o);
+      sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    }
+    const float target = fminf(2.f * k + 64.f, 0.5f * (k + kStreamCap));
+    const float p = target / (float)nv;
+    if (n > 1.f && p < 1.f) {
+      const float mean = sum / n;
+      const float sd = sqrtf(fmaxf(sq / n - mean * mean, 0.f));
+      if (sd > 0.f) thr = mean + 1.41421356f * erfcinvf(2.f * p) * sd;
+    }
+  }
+  if (lane == 0) {
+    ws.thr[q] = thr;
+    ws.cnt[q] = 0u;
+  }
+}
+
+// Exact top k of a query's list, or queue the query for the fallback.
+template <int NT>
+__global__ void __launch_bounds__(NT)
+stream_select_kernel(Batch b, int64_t max_len, int k, StreamWs ws, int32_t *__restrict__ idx,
+                     int32_t *__restrict__ count) {
+  __shared__ RegShared<NT> sh;
+  const int q = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const uint32_t c = ws.cnt[q];
+  const bool all = ws.thr[q] == -INFINITY;   // every visible entry was offered
+  if (c > (uint32_t)kStreamCap || (!all && c < (uint32_t)k)) {
+    if (t == 0) ws.fb_rows[atomicAdd(&ws.hdr[0], 1u)] = q;
+    return;
+  }
+  for (int i = t; i < 256; i += NT) sh.hist[i] = 0u;
+  const int n = (int)c;
+  uint32_t mn = 0xffffffffu, mx = 0u, ne = 0u;
+  for (int i = t; i < n; i += NT) {
+    const int64_t o = (int64_t)q * kStreamCap + i;
+    const uint32_t key = score_key(ws.val[o]);
+    sh.list_key[i] = key;
+    sh.list_pos[i] = ws.ent[o];
+    if (key != 0u) {
+      mn = min(mn, key);
+      mx = max(mx, key);
+      ++ne;
+    }
+  }
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  ne = __reduce_add_sync(0xffffffffu, ne);
+  if (lane == 0) {
+    sh.red[0][warp] = mn;
+    sh.red[1][warp] = mx;
+    sh.red[2][warp] = ne;
+  }
+  if (t == 0) sh.out_count = 0u;
+  __syncthreads();
+  mn = 0xffffffffu;
+  mx = 0u;
+  ne = 0u;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    mn = min(mn, sh.red[0][w]);
+    mx = max(mx, sh.red[1][w]);
+    ne += sh.red[2][w];
+  }
+  int32_t *out = idx + (int64_t)q * k;
+  uint32_t got;
+  if (ne <= (uint32_t)k) {
+    for (int i0 = 0; i0 < n; i0 += NT) {
+      const int i = i0 + t;
+      const bool take = i < n && sh.list_key[i] != 0u;
+      const uint32_t slot = warp_reserve(take, &sh.out_count);
+      if (take) out[slot] = sh.list_pos[i];
+    }
+    got = ne;
+  } else {
+    select_listed<NT>(n, mn, mx, (uint32_t)k, sh,
+                      [&](int i, uint32_t slot) { out[slot] = sh.list_pos[i]; });
+    got = (uint32_t)k;
+  }
+  for (int i = (int)got + t; i < k; i += NT) out[i] = -1;
+  if (t == 0) count[q] = (int32_t)got;
+}
+
+// MXFP4 row segment (32 elements = 16 bytes of codes, one power-of-two scale)
+// decoded exactly to fp32
+__device__ __forceinline__ void mx_decode32(const uint8_t *codes, float scale, float (&v)[32]) {
+  const uint4 c = __ldg(reinterpret_cast<const uint4 *>(codes));
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t h[4];
+    e2m1x8_f16x8(w[i], h);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __half2 x = *reinterpret_cast<const __half2 *>(&h[j]);
+      v[8 * i + 2 * j] = __low2float(x) * scale;
+      v[8 * i + 2 * j + 1] = __high2float(x) * scale;
+    }
+  }
+}
+
+constexpr int kFbBlock = 1024;   // entries rescored per round of the fallback
+
+// Fallback rows: the whole row rescored on the CUDA cores in rounds of
+// kFbBlock entries, each round merged with the running top k (kept in the
+// list arrays) by the exact list selection.  Per-head dots in fp32 (exact for
+// MXFP4 operands whose group sums fit 24 bits, as the tensor-core dots are),
+// then the scoring epilogue's own head combination: (w/2) * (x + |x|) summed
+// in four chains by head index mod 4, 32 heads per chain segment.
+template <int HI>
+__global__ void __launch_bounds__(256)
+stream_fallback_kernel(Batch b, int64_t max_len, int k, const uint8_t *__restrict__ q_fp4,
+                       const float *__restrict__ q_scale, const float *__restrict__ head_w,
+                       const uint8_t *__restrict__ k_fp4, const float *__restrict__ k_scale,
+                       StreamWs ws, int32_t *__restrict__ idx, int32_t *__restrict__ count) {
+  constexpr int NT = 256;
+  __shared__ RegShared<NT> sh;
+  __shared__ float w2[HI];
+  __shared__ int row_slot;
+  // dynamic: the query dequantised [HI][128] f32, then the merge's output
+  // (keys and entries of up to 2048 pairs)
+  extern __shared__ __align__(16) uint32_t fb_dyn[];
+  float *qv = reinterpret_cast<float *>(fb_dyn);
+  uint32_t *tmp_key = fb_dyn + HI * 128;
+  int32_t *tmp_ent = reinterpret_cast<int32_t *>(tmp_key + 2048);
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  for (int i = t; i < 256; i += NT) sh.hist[i] = 0u;
+  while (true) {
+    __syncthreads();
+    if (t == 0) row_slot = (int)atomicAdd(&ws.hdr[1], 1u);
+    __syncthreads();
+    const int slot = row_slot;
+    if (slot >= (int)ws.hdr[0]) break;
+    const int q = ws.fb_rows[slot];
+    const int64_t nv = stream_nvis(b, q, max_len);
+    const int64_t kv0 = b.kv_start[b.q_req[q]];
+    for (int i = t; i < HI * 4; i += NT) {   // 32-element segments of the query
+      float v[32];
+      mx_decode32(q_fp4 + ((int64_t)q * HI) * 64 + i * 16, q_scale[(int64_t)q * HI * 4 + i], v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) qv[i * 32 + j] = v[j];
+    }
+    for (int h = t; h < HI; h += NT) w2[h] = 0.5f * (head_w ? head_w[(int64_t)q * HI + h] : 1.f);
+    __syncthreads();
+    int n_cur = 0;
+    for (int64_t s0 = 0; s0 < nv; s0 += kFbBlock) {
+      const int nb = (int)min((int64_t)kFbBlock, nv - s0);
+      for (int i = t; i < nb; i += NT) {
+        const int64_t j = s0 + i;
+        const uint8_t *kc = k_fp4 + (kv0 + j) * 64;
+        const float *ks = k_scale + (kv0 + j) * 4;
+        float dot[HI];
+#pragma unroll
+        for (int h = 0; h < HI; ++h) dot[h] = 0.f;
+#pragma unroll 1
+        for (int g = 0; g < 4; ++g) {
+          float kx[32];
+          mx_decode32(kc + g * 16, __ldg(ks + g), kx);
+#pragma unroll
+          for (int h = 0; h < HI; ++h) {
+#pragma unroll
+            for (int d = 0; d < 32; ++d) dot[h] = fmaf(qv[h * 128 + g * 32 + d], kx[d], dot[h]);
+          }
+        }
+        float acc = 0.f;
+        constexpr int LW = HI < 32 ? HI : 32;
+#pragma unroll
+        for (int l = 0; l < HI / LW; ++l) {
+          float a0 = acc, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+          for (int h = l * LW; h < l * LW + LW; h += 4) {
+            a0 = fmaf(w2[h], dot[h] + fabsf(dot[h]), a0);
+            a1 = fmaf(w2[h + 1], dot[h + 1] + fabsf(dot[h + 1]), a1);
+            a2 = fmaf(w2[h + 2], dot[h + 2] + fabsf(dot[h + 2]), a2);
+            a3 = fmaf(w2[h + 3], dot[h + 3] + fabsf(dot[h + 3]), a3);
+          }
+          acc = (a0 + a1) + (a2 + a3);
+        }
+        sh.list_key[n_cur + i] = score_key(acc);
+        sh.list_pos[n_cur + i] = (int32_t)j;
+      }
+      __syncthreads();
+      // merge: the k best of the running set and this round
+      const int n = n_cur + nb;
+      uint32_t mn = 0xffffffffu, mx = 0u, ne = 0u;
+      for (int i = t; i < n; i += NT) {
+        const uint32_t key = sh.list_key[i];
+        if (key != 0u) {
+          mn = min(mn, key);
+          mx = max(mx, key);
+          ++ne;
+        }
+      }
+      mn = __reduce_min_sync(0xffffffffu, mn);
+      mx = __reduce_max_sync(0xffffffffu, mx);
+      ne = __reduce_add_sync(0xffffffffu, ne);
+      if (lane == 0) {
+        sh.red[0][warp] = mn;
+        sh.red[1][warp] = mx;
+        sh.red[2][warp] = ne;
+      }
+      if (t == 0) sh.out_count = 0u;
+      __syncthreads();
+      mn = 0xffffffffu;
+      mx = 0u;
+      ne = 0u;
+#pragma unroll
+      for (int w = 0; w < NT / 32; ++w) {
+        mn = min(mn, sh.red[0][w]);
+        mx = max(mx, sh.red[1][w]);
+        ne += sh.red[2][w];
+      }
+      auto keep = [&](int i, uint32_t slot) {
+        tmp_key[slot] = sh.list_key[i];
+        tmp_ent[slot] = sh.list_pos[i];
+      };
+      if (ne <= (uint32_t)k) {
+        for (int i0 = 0; i0 < n; i0 += NT) {
+          const int i = i0 + t;
+          const bool take = i < n && sh.list_key[i] != 0u;
+          const uint32_t sl = warp_reserve(take, &sh.out_count);
+          if (take) keep(i, sl);
+        }
+        __syncthreads();
+        n_cur = (int)ne;
+      } else {
+        select_listed<NT>(n, mn, mx, (uint32_t)k, sh, keep);
+        n_cur = k;
+      }
+      __syncthreads();
+      for (int i = t; i < n_cur; i += NT) {
+        sh.list_key[i] = tmp_key[i];
+        sh.list_pos[i] = tmp_ent[i];
+      }
+      __syncthreads();
+    }
+    int32_t *out = idx + (int64_t)q * k;
+    for (int i = t; i < k; i += NT) out[i] = i < n_cur ? sh.list_pos[i] : -1;
+    if (t == 0) count[q] = n_cur;
+  }
+}
+
 }  // namespace
 
 int topk_launch(const Batch &b, const float *scores, int64_t ld, int k,
@@ -841,6 +1153,35 @@ int topk_launch(const Batch &b, const float *scores, int64_t ld, int k,
     candidate_blocks_kernel<<<b.num_q, kThreads, smem_b, st>>>(
         b, scores, ld, block, max_blocks, blocks_out, nblocks_out,
         nblk < kSmemKeys ? nblk : (int64_t)kSmemKeys);
+  }
+  return launch_status();
+}
+
+int stream_threshold_launch(const Batch &b, int64_t max_len, int k, int stride,
+                            const StreamWs &ws, cudaStream_t st) {
+  stream_threshold_kernel<<<(b.num_q + 7) / 8, 256, 0, st>>>(b, max_len, k, stride, ws);
+  return launch_status();
+}
+
+int stream_select_launch(const Batch &b, int64_t max_len, int k, int n_heads,
+                         const uint8_t *q_fp4, const float *q_scale, const float *head_w,
+                         const uint8_t *k_fp4, const float *k_scale, const StreamWs &ws,
+                         int32_t *idx, int32_t *count, cudaStream_t st) {
+  stream_select_kernel<256><<<b.num_q, 256, 0, st>>>(b, max_len, k, ws, idx, count);
+  // the fallback: one persistent CTA per SM takes queued rows until none is left
+  const int grid = sm_count();
+  auto fb = [&](auto kern, int hi) {
+    const int smem = (hi * 128 + 2 * 2048) * 4;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    kern<<<grid, 256, smem, st>>>(b, max_len, k, q_fp4, q_scale, head_w, k_fp4, k_scale, ws,
+                                  idx, count);
+  };
+  switch (n_heads) {
+    case 8: fb(stream_fallback_kernel<8>, 8); break;
+    case 16: fb(stream_fallback_kernel<16>, 16); break;
+    case 32: fb(stream_fallback_kernel<32>, 32); break;
+    case 64: fb(stream_fallback_kernel<64>, 64); break;
+    default: return CSA2_ERR_UNSUPPORTED;
   }
   return launch_status();
 }
