@@ -42,7 +42,7 @@ def lib():
                      "oracle_topk_candidates", "oracle_sparse_swa_attn",
                      "oracle_sparse_swa_attn_fp4kv", "oracle_encoder_replay_layout",
                      "oracle_rows_gather", "oracle_rows_scatter", "oracle_encode_rows",
-                     "oracle_encode_e4m3", "oracle_encode_e2m1"):
+                     "oracle_encode_e4m3", "oracle_encode_e2m1", "oracle_index_k_project"):
             getattr(_lib, name).restype = C.c_int
         _lib.oracle_decode_fp4kv_row.restype = None
         _lib.oracle_decode_mxfp4_row.restype = None
@@ -186,6 +186,25 @@ def encode_rows(fmt, src, dst_row, codes, scales):
     err = lib().oracle_encode_rows(C.c_int(fmt), C.c_int64(n), _p(x), C.c_int(dim), _p(dr),
                                    _p(cd), _p(sc), C.c_int64(cd.shape[0]))
     return cd, sc, err
+
+
+def index_k_project(x_bf16, w_bf16, dst_row, codes, scales):
+    """Index keys projected from bf16 rows x [n, dim_in] by bf16 weights w
+    [dim_out, dim_in], written as MXFP4 rows dst_row of copies of (codes,
+    scales).  Inputs are the raw bf16 bit patterns (uint16).  Returns (codes,
+    scales, y fp32 [n, dim_out] before quantisation, err)."""
+    x = _c(x_bf16, np.uint16)
+    w = _c(w_bf16, np.uint16)
+    n, dim_in = x.shape
+    dim_out = w.shape[0]
+    dr = _c(dst_row, np.int64)
+    cd = np.array(codes, copy=True, order="C")
+    sc = np.array(scales, copy=True, order="C")
+    y = np.zeros((n, dim_out), np.float32)
+    err = lib().oracle_index_k_project(C.c_int64(n), _p(x), C.c_int(dim_in), _p(w),
+                                       C.c_int(dim_out), _p(dr), _p(cd), _p(sc),
+                                       C.c_int64(cd.shape[0]), _p(y))
+    return cd, sc, y, err
 
 
 def index_score(b, q_fp4, q_scale, head_w, k_fp4, k_scale, ld,

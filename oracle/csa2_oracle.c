@@ -20,11 +20,11 @@
  *                    the card's own layout, E2M1 with one E4M3 scale per 16
  *                    channels (288 B per entry); SWA rows stay FP8.
  *   index score      same page, CSA2 and Hierarchical Sparse Indexer cards; SGLang/
- *                    Miles day-0 article (theainews.cc) sec. 2 and sec. 5 ("FP4
- *                    索引与 TP 布局": MQA-shaped indexer, heads replicated, a
+ *                    Miles day-0 article (theainews.cc) sec. 2 and sec. 5 (the FP4
+ *                    indexer and its TP layout: MQA-shaped, heads replicated, a
  *                    score all-reduce would be needed if heads were sharded).
  *                    Reading: s(q,j) = sum_h w[q,h] * ReLU(<Qi[q,h], Ki[j]>).
- *   visibility       CSA2 card ("压缩器也改了"): non-overlapping groups of m
+ *   visibility       CSA2 card, compressor paragraph: non-overlapping groups of m
  *                    tokens; entry j is complete, hence visible to the query at
  *                    absolute position t, once its last token m*j+m-1 <= t,
  *                    i.e. n_vis(t) = floor((t+1)/m).
@@ -46,8 +46,9 @@
  *                    (the other rows are left as they were).
  *   cache writes     mixed-precision card (main KV FP8 block-32 or E2M1 with an
  *                    E4M3 scale per 16, index K MXFP4 per 32) and article sec.
- *                    5 ("保持量化语义的融合": a fused quantise-and-write keeps
- *                    the rounding sequence of the unfused one).  Reading: the
+ *                    5, on fusions that keep the quantisation semantics: a
+ *                    fused quantise-and-write keeps the rounding sequence of
+ *                    the unfused one.  Reading: the
  *                    group scale is computed in fp32, x / scale in fp32, and
  *                    the element rounds to nearest (ties to even) with
  *                    saturation at the format's largest finite value.
@@ -245,6 +246,36 @@ static double bf16_to_double(uint16_t h) {
   float f;
   memcpy(&f, &u, 4);
   return (double)f;
+}
+
+/* Index keys projected from the compressed main KV, written as MXFP4 cache
+ * rows ("DeepSeek V4.1 Flash 建模", CSA2 card, compressor paragraph: index K is
+ * projected from the compressed main KV; SGLang/Miles day-0 article sec. 5:
+ * projection weights in BF16 with FP32 accumulation).  For source row i
+ * (x: dim_in bf16 values) and output channel o (w row o: dim_in bf16 values):
+ *   y[i][o] = sum_d x[i][d] * w[o][d]
+ * formed in double (every bf16 x bf16 product is exact there, and so is the
+ * sum while the products span fewer than about 37 binades) and rounded once
+ * to fp32: the value an fp32 accumulation approximates.  The rows y[i] are
+ * then encoded exactly as oracle_encode_rows format 3 (MXFP4) encodes rows,
+ * into row dst_row[i] of (codes, scales).  y_out ([n, dim_out] fp32) receives
+ * the unquantised rows when not NULL. */
+int oracle_index_k_project(int64_t n, const uint16_t *x_bf16, int dim_in,
+                           const uint16_t *w_bf16, int dim_out, const int64_t *dst_row,
+                           uint8_t *codes, float *scales, int64_t rows, float *y_out) {
+  float *y = (float *)malloc(sizeof(float) * (size_t)(n > 0 ? n : 1) * (size_t)dim_out);
+  for (int64_t i = 0; i < n; ++i) {
+    for (int o = 0; o < dim_out; ++o) {
+      double acc = 0.0;
+      for (int d = 0; d < dim_in; ++d)
+        acc += bf16_to_double(x_bf16[i * dim_in + d]) * bf16_to_double(w_bf16[(int64_t)o * dim_in + d]);
+      y[i * dim_out + o] = (float)acc;
+    }
+  }
+  if (y_out) memcpy(y_out, y, sizeof(float) * (size_t)n * (size_t)dim_out);
+  const int err = oracle_encode_rows(3, n, y, dim_out, dst_row, codes, scales, rows);
+  free(y);
+  return err;
 }
 
 uint16_t oracle_double_to_bf16(double x) {
