@@ -67,6 +67,12 @@ MUTANTS = [
      ["test_oracle_index.py"]),
     ("block_tie_order_reversed", "return (x->b > y->b) - (x->b < y->b);",
      "return (x->b < y->b) - (x->b > y->b);", ["test_oracle_select.py"]),
+    ("project_drops_last_channel", "for (int d = 0; d < dim_in; ++d)",
+     "for (int d = 0; d < dim_in - 1; ++d)", ["test_oracle_project.py"]),
+    ("project_weight_row_offset", "w_bf16[(int64_t)o * dim_in + d]",
+     "w_bf16[(int64_t)((o + 1) % dim_out) * dim_in + d]", ["test_oracle_project.py"]),
+    ("project_rounds_twice", "y[i * dim_out + o] = (float)acc;",
+     "y[i * dim_out + o] = (float)(float)(acc + 0x1p-30);", ["test_oracle_project.py"]),
 ]
 
 
