@@ -341,12 +341,60 @@ def bench_headline(args, rank, world, local_rank):
             index[key] = round(is_tflops / peaks[name]["tflops"], 4)
     topk = {"kernel": "csa2_topk", "avg_launch_ms": round(kern["select"], 4),
             "share_of_step": share["select"]}
+    streamed = bench_streamed(args, w, run, stream, flush, dev, world)
     e2e = None
     if not args.no_e2e:
         e2e = bench_e2e(args, w, run, dev, rank, world, headline=True)
     return dict(value=value, ms=ms, wall=wall, clocks=clk, roofline=roofline, e2e=e2e,
                 launches=3 * args.steps, rows=run.nq, w=w, index=index, topk=topk,
-                peaks=peaks)
+                peaks=peaks, streamed=streamed)
+
+
+def bench_streamed(args, w, run, stream, flush, dev, world):
+    """The same Full layer with the index score streamed into the top-K
+    (csa2_index_topk: sample pass, threshold, appending scoring pass, list
+    selection, fallback) instead of a score row per query and a separate
+    top-K; attention unchanged.  Events around each launch group."""
+    import torch
+    import sparse_attention_prefill_gb300 as S
+    b, L = run.batches["full"], w.layers["full"]
+    need = S.csa2_index_topk_workspace(run.nq, w.ld)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    idx = torch.empty_like(run.idx["full"])
+    cnt = torch.empty_like(run.count["full"])
+    args_ = (b, run._lt("full", "q_fp4"), run._lt("full", "q_scale"), run._lt("full", "head_w"),
+             w.pool.k_fp4, w.pool.k_scale, w.ld, w.topk)
+
+    def step(ev=None):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)] if ev is not None else None
+        if e:
+            e[0].record(stream)
+        S.index_topk(*args_, idx=idx, count=cnt, workspace=ws, d_err=run.d_err)
+        if e:
+            e[1].record(stream)
+        run.attend("full", idx)
+        if e:
+            e[2].record(stream)
+            ev.append(e)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    ev = []
+    for _ in range(max(5, min(args.steps, 50))):
+        flush.zero_()
+        step(ev)
+    torch.cuda.synchronize()
+    assert int(run.d_err.item()) == 0
+    sel = sum(e[0].elapsed_time(e[1]) for e in ev) / len(ev)
+    att = sum(e[1].elapsed_time(e[2]) for e in ev) / len(ev)
+    ms = max_over_ranks(sel + att, dev, world)
+    # the selection equals the unstreamed chain's on these rows
+    same = bool((torch.sort(idx, 1).values == torch.sort(run.idx["full"], 1).values).all())
+    return {"kernels": "csa2_index_topk + csa2_sparse_swa_attn", "ms_per_step": round(ms, 4),
+            "value": round(split_queries_per_s(w.num_q, 1, ms), 1),
+            "index_topk_ms": round(sel, 4), "attention_ms": round(att, 4),
+            "workspace_bytes": int(need), "same_selection_as_unstreamed": same}
 
 
 def bench_fp4kv(args, w, run, stream, flush, hbm):
@@ -471,6 +519,31 @@ def bench_quant(args, w, stream, flush, hbm):
                       "achieved_gbs": round(byts / (ms * 1e-3) / 1e9, 1),
                       "frac": round(byts / (ms * 1e-3) / 1e9 / hbm, 4)})
         del src, codes, scales
+    # the index keys of the same entries projected from their bf16 latent rows
+    # (512 -> 128, tensor cores) and written as MXFP4 rows in the same kernel
+    x = torch.randn((n, 512), generator=g, device=dev).to(torch.bfloat16)
+    wt = (torch.randn((128, 512), generator=g, device=dev) / 512 ** 0.5).to(torch.bfloat16)
+    codes = torch.empty((n, 64), dtype=torch.uint8, device=dev)
+    scales = torch.empty((n, 4), dtype=torch.float32, device=dev)
+    fn = lambda: S.index_k_project(x, wt, dst, codes, scales, d_err=d_err)   # noqa: E731
+    for _ in range(3):
+        fn()
+    ts = []
+    for _ in range(max(5, min(args.steps, 20))):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ts) / len(ts)
+    byts = n * (512 * 2 + 8 + 64 + 16) + 128 * 512 * 2
+    cases.append({"case": "index_k_project_mxfp4", "kernel": "csa2_index_k_project", "rows": n,
+                  "avg_launch_ms": round(ms, 4), "algorithmic_bytes_per_launch": int(byts),
+                  "flops": 2 * n * 512 * 128,
+                  "achieved_gbs": round(byts / (ms * 1e-3) / 1e9, 1),
+                  "frac": round(byts / (ms * 1e-3) / 1e9 / hbm, 4)})
     assert int(d_err.item()) == 0
     return {"kernel": "csa2_quantize_rows", "peak_gbs": hbm, "cases": cases}
 
@@ -1062,7 +1135,8 @@ def main():
                 "clocks": r["clocks"], "gpu_launches": r["launches"],
                 "wall_s_timed_region": round(r["wall"], 4),
                 "index_score": idx, "index_score_frac_of_fp4_peak": idx.get("frac_of_fp4_peak"),
-                "topk": r["topk"], "tensor_peaks_tflops": r["peaks"],
+                "topk": r["topk"], "streamed_score_topk": r["streamed"],
+                "tensor_peaks_tflops": r["peaks"],
                 "c2_decoder_replay": c2}
         print(json.dumps(line))
     if world > 1:

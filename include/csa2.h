@@ -373,6 +373,31 @@ CSA2_API int csa2_rows_scatter(const int32_t *count, int64_t capacity,
                          csa2_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * NEXT-2b. Index keys projected from the compressed main KV, written as MXFP4
+ * cache rows   [CSA2] CSA2 card (compressor paragraph: the index K is
+ * projected from the compressed main KV); [D0] sec. 5 (projection weights in
+ * BF16 with FP32 accumulation; a fused quantise/pack/cache write keeps the
+ * unfused rounding).
+ *
+ * For i < n:  y[i, o] = sum_d x[i, d] * w[o, d]  (fp32 accumulation on the
+ * tensor cores), then row dst_row[i] of (k_fp4, k_scale) <- the MXFP4 encoding
+ * of y[i, :] exactly as csa2_quantize_rows(CSA2_FMT_MXFP4) encodes an fp32
+ * row.  Negative dst_row entries are skipped; entries >= rows are skipped and
+ * flagged (CSA2_DERR_RANGE_ROW); groups with a NaN or infinity are written as
+ * zeros (CSA2_DERR_NONFINITE); scales outside [2^-23, 2^12] set
+ * CSA2_DERR_SCALE.  The pages leave the pooling of a ratio-2 pair and the
+ * RoPE channels undefined: x is the compressed latent row as the caller
+ * forms it, and no rotation is applied.
+ *   x_bf16  [n, dim_in] bf16 (16-byte aligned);  w_bf16 [dim_out, dim_in] bf16
+ *   k_fp4   [rows, dim_out/2] (16-byte aligned); k_scale [rows, dim_out/32] fp32
+ * Supported: dim_in == 512, dim_out == 128.
+ * ------------------------------------------------------------------------- */
+CSA2_API int csa2_index_k_project(int64_t n, const void *x_bf16, int32_t dim_in,
+                                  const void *w_bf16, int32_t dim_out,
+                                  const int64_t *dst_row, uint8_t *k_fp4, float *k_scale,
+                                  int64_t rows, int32_t *d_err, csa2_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Quantise-and-write of cache rows   [CSA2] mixed-precision card (main KV FP8
  * block-32, or E2M1 with one E4M3 scale per 16 channels; index K MXFP4 per
  * 32); [D0] sec. 5, on fusions that keep the quantisation semantics: fusing

@@ -30,7 +30,7 @@ EXPORTED = ("csa2_status_string", "csa2_tail_layout", "csa2_index_score", "csa2_
             "csa2_topk_candidates", "csa2_sparse_swa_attn", "csa2_sparse_swa_attn_fp4kv",
             "csa2_encoder_replay_layout", "csa2_rows_gather", "csa2_rows_scatter",
             "csa2_quantize_rows", "csa2_set_wait_limit_ns", "csa2_index_topk_workspace",
-            "csa2_index_topk")
+            "csa2_index_topk", "csa2_index_k_project")
 
 
 class Csa2Error(RuntimeError):
@@ -76,6 +76,7 @@ def load(path: Optional[str] = None):
     lib.csa2_quantize_rows.argtypes = [i32, i64, vp, i32, vp, vp, vp, i64, vp, vp]
     lib.csa2_set_wait_limit_ns.argtypes = [C.c_uint64]
     lib.csa2_index_topk_workspace.argtypes = [i32, i64, vp]
+    lib.csa2_index_k_project.argtypes = [i64, vp, i32, vp, i32, vp, vp, vp, i64, vp, vp]
     lib.csa2_index_topk.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, i64, i32, vp, vp, vp, i64,
                                     vp, vp]
     for name in EXPORTED[1:]:
@@ -100,6 +101,21 @@ def csa2_index_topk(batch, n_heads, head_dim, q_fp4, q_scale, head_w, k_fp4, k_s
                                   _ptr(q_scale), _ptr(head_w), _ptr(k_fp4), _ptr(k_scale),
                                   int(max_len), int(k), _ptr(idx), _ptr(count), _ptr(workspace),
                                   int(workspace_bytes), _ptr(d_err), _stream(stream))
+
+
+def csa2_index_k_project(n, x_bf16, dim_in, w_bf16, dim_out, dst_row, k_fp4, k_scale, rows,
+                         d_err, stream=None) -> int:
+    return load().csa2_index_k_project(int(n), _ptr(x_bf16), int(dim_in), _ptr(w_bf16),
+                                       int(dim_out), _ptr(dst_row), _ptr(k_fp4), _ptr(k_scale),
+                                       int(rows), _ptr(d_err), _stream(stream))
+
+
+def index_k_project(x, w, dst_row, k_fp4, k_scale, d_err=None, stream=None):
+    """Project bf16 rows x [n, 512] by bf16 weights w [128, 512] and write the
+    results as MXFP4 index-key rows dst_row of (k_fp4 [rows, 64], k_scale
+    [rows, 4]) in place."""
+    _check(csa2_index_k_project(x.shape[0], x, x.shape[1], w, w.shape[0], dst_row, k_fp4,
+                                k_scale, k_fp4.shape[0], d_err, stream), "csa2_index_k_project")
 
 
 def csa2_set_wait_limit_ns(ns: int) -> int:

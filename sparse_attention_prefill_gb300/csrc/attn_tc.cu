@@ -41,11 +41,10 @@
 // otherwise); on expiry the kernel raises CSA2_DERR_TIMEOUT, drains its MMAs
 // and any Q copy in flight (each for at most two seconds), frees TMEM and
 // returns.
-#include <cuda.h>   // CUtensorMap (the encoder is reached through the runtime)
-
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tcgen05.cuh"
+#include "tma.cuh"
 
 namespace csa2 {
 namespace {
@@ -881,28 +880,6 @@ attn_tc_kernel(Params P, const __grid_constant__ CUtensorMap tmap_q) {
     fence_after_sync();
     tmem_dealloc(ms->tmem_base, kTmemCols);
   }
-}
-
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
-// against the driver library)
-using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// looked up once; the initialisation of a function-local static is
-// thread-safe, so concurrent first calls all see the finished lookup
-EncodeTiled encode_tiled() {
-  static const EncodeTiled fn = []() -> EncodeTiled {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult res;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &res) == cudaSuccess &&
-        res == cudaDriverEntryPointSuccess)
-      return reinterpret_cast<EncodeTiled>(p);
-    return nullptr;
-  }();
-  return fn;
 }
 
 // Q [num_q, n_heads, 512] bf16 as a 3-D map (dims, heads, queries) with

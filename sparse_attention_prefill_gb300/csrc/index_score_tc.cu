@@ -358,7 +358,7 @@ __device__ void mma_role(const Params &P, uint8_t *smem, Misc *ms, int y) {
   __syncwarp();
 }
 
-template <int HI>
+template <int HI, bool kList>
 __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, int y) {
   const CandView cv = cand_view(P, ms, smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -390,7 +390,7 @@ __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
           const int64_t j = ru.gather ? cv.entry(ql, q0 + ql, s) : s;
           if (j >= ms->n_vis[ql]) outv = -INFINITY;
         }
-        if (P.list_cnt == nullptr) {
+        if constexpr (!kList) {
           if (in) P.scores[(int64_t)(q0 + ql) * P.out_ld + col] = outv;
           return;
         }
@@ -469,7 +469,7 @@ __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
   }
 }
 
-template <int HI>
+template <int HI, bool kList>
 __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Misc *ms = reinterpret_cast<Misc *>(smem + kOffMisc);
@@ -665,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
     fence_after_sync();
   }
   if (warp < kEpiWarps) {
-    epilogue_role<HI>(P, smem, ms, q0, y);
+    epilogue_role<HI, kList>(P, smem, ms, q0, y);
   } else if (warp == kMmaWarp) {
     mma_role(P, smem, ms, y);
   } else {
@@ -696,11 +696,17 @@ int launch(Params &P, int n_heads, cudaStream_t st) {
   if (chunks > 65535) return CSA2_ERR_UNSUPPORTED;
   const int64_t tiles = (P.b.num_q + P.qt - 1) / P.qt;
   dim3 grid((unsigned)tiles, (unsigned)chunks);
-#define CSA2_LAUNCH(H)                                                                     \
-  do {                                                                                     \
-    cudaFuncSetAttribute(index_score_tc_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                         (int)kSmemBytes);                                                 \
-    index_score_tc_kernel<H><<<grid, kThreads, kSmemBytes, st>>>(P);                       \
+#define CSA2_LAUNCH(H)                                                                       \
+  do {                                                                                       \
+    if (P.list_cnt) {                                                                        \
+      cudaFuncSetAttribute(index_score_tc_kernel<H, true>,                                   \
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);    \
+      index_score_tc_kernel<H, true><<<grid, kThreads, kSmemBytes, st>>>(P);                 \
+    } else {                                                                                 \
+      cudaFuncSetAttribute(index_score_tc_kernel<H, false>,                                  \
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);    \
+      index_score_tc_kernel<H, false><<<grid, kThreads, kSmemBytes, st>>>(P);                \
+    }                                                                                        \
   } while (0)
   switch (n_heads) {
     case 8: CSA2_LAUNCH(8); break;

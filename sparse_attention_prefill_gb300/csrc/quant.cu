@@ -31,20 +31,6 @@ __device__ __forceinline__ uint32_t e4m3x2(float x0, float x1) {
   return r;
 }
 
-// 8 x fp32 -> 8 x E2M1 nibbles (element 2i in the low nibble of byte i)
-__device__ __forceinline__ uint32_t e2m1x8(const float *x) {
-  uint32_t r;
-  asm("{ .reg .b8 t0, t1, t2, t3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n\t"
-      "mov.b32 %0, {t0, t1, t2, t3}; }"
-      : "=r"(r)
-      : "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]), "f"(x[7]));
-  return r;
-}
-
 // value of an E4M3 code (exact, through f16)
 __device__ __forceinline__ float e4m3_to_float(uint32_t code) {
   uint32_t h;

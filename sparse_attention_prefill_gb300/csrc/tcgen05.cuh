@@ -69,6 +69,11 @@ __host__ __device__ constexpr uint32_t make_idesc_f16(uint32_t m, uint32_t n, bo
          ((m >> 4) << 24);
 }
 
+// The same for bf16 A and B (format code 1 in both fields).
+__host__ __device__ constexpr uint32_t make_idesc_bf16(uint32_t m, uint32_t n) {
+  return make_idesc_f16(m, n, false, false) | (1u << 7) | (1u << 10);
+}
+
 // ---------------------------------------------------------------------------
 // TMEM allocation (one full warp executes these)
 // ---------------------------------------------------------------------------
@@ -285,6 +290,17 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, 
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// TMA: one box of a 2-D tensor map into shared memory, completing on `bar`
+// (same alignment rules as tma_load_3d).
+__device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, int y,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
 
