@@ -63,6 +63,7 @@ typedef struct CUstream_st *csa2_stream_t; /* same object as cudaStream_t */
 #define CSA2_ERR_UNSUPPORTED 2 /* valid request this build does not implement */
 #define CSA2_ERR_CUDA 3        /* a kernel launch failed */
 #define CSA2_ERR_TIMEOUT 4     /* reserved (device waits report CSA2_DERR_TIMEOUT) */
+#define CSA2_ERR_TOO_LARGE 5   /* the request needs more scratch than the fixed array holds */
 
 /* data-error bits ORed into *d_err */
 #define CSA2_DERR_RANGE_IDX 1     /* a selected index outside [0, n_vis) or past kv_len */
@@ -253,6 +254,37 @@ CSA2_API int csa2_index_topk(const csa2_batch *b, int32_t n_heads, int32_t head_
                              int32_t *idx, int32_t *count, void *workspace,
                              int64_t workspace_bytes, int32_t *d_err,
                              csa2_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * csa2_index_topk without a workspace argument, for callers that cannot
+ * allocate device memory: code that runs while a CUDA graph is being
+ * captured, a memory pool's own set-up code, or a host runtime that forbids
+ * cudaMalloc after start-up.  The pages have no counterpart to this call; it
+ * runs exactly csa2_index_topk's kernels and gives the same results.
+ *
+ * Its scratch is one fixed array of 64 MiB inside the library (the size is
+ * csa2_index_topk_static_capacity's answer), reserved on every GPU that loads
+ * the library until the process exits.  A request whose scratch
+ * (csa2_index_topk_workspace(num_q, max_len)) exceeds it is rejected with
+ * CSA2_ERR_TOO_LARGE and nothing is launched.  The call allocates nothing
+ * (no cudaMalloc, no allocating library routine).
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and keeps it; make that first call before any
+ *    stream capture, since the lookup is a runtime call of its own.
+ *  - Every call, from any thread or stream, uses the same array, which keeps
+ *    whatever the last call left there; each call initialises what it needs
+ *    (its counters and queue are cleared by its first kernel), so leftovers
+ *    never change a result.  Calls that overlap on the GPU race on the array
+ *    and their results are undefined: order them (one stream, or events).
+ * Arguments, outputs and flags as csa2_index_topk.
+ * ------------------------------------------------------------------------- */
+CSA2_API int csa2_index_topk_static_capacity(int64_t *bytes);
+CSA2_API int csa2_index_topk_static(const csa2_batch *b, int32_t n_heads, int32_t head_dim,
+                                    const uint8_t *q_fp4, const float *q_scale,
+                                    const float *head_w, const uint8_t *k_fp4,
+                                    const float *k_scale, int64_t max_len, int32_t k,
+                                    int32_t *idx, int32_t *count, int32_t *d_err,
+                                    csa2_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * a8-a10. Sparse + sliding-window attention under one softmax

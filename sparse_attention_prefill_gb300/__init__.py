@@ -20,7 +20,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libcsa2.so")
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_TOO_LARGE = 0, 1, 2, 3, 4, 5
 DERR_RANGE_IDX, DERR_RANGE_WINDOW, DERR_RANGE_CTX = 1, 2, 4
 DERR_SCALE, DERR_LD, DERR_CAPACITY, DERR_BAD_EXTEND = 8, 16, 32, 64
 DERR_TIMEOUT, DERR_RANGE_ROW, DERR_NONFINITE = 128, 256, 512
@@ -30,7 +30,8 @@ EXPORTED = ("csa2_status_string", "csa2_tail_layout", "csa2_index_score", "csa2_
             "csa2_topk_candidates", "csa2_sparse_swa_attn", "csa2_sparse_swa_attn_fp4kv",
             "csa2_encoder_replay_layout", "csa2_rows_gather", "csa2_rows_scatter",
             "csa2_quantize_rows", "csa2_set_wait_limit_ns", "csa2_index_topk_workspace",
-            "csa2_index_topk", "csa2_index_k_project")
+            "csa2_index_topk", "csa2_index_k_project", "csa2_index_topk_static_capacity",
+            "csa2_index_topk_static")
 
 
 class Csa2Error(RuntimeError):
@@ -77,6 +78,9 @@ def load(path: Optional[str] = None):
     lib.csa2_set_wait_limit_ns.argtypes = [C.c_uint64]
     lib.csa2_index_topk_workspace.argtypes = [i32, i64, vp]
     lib.csa2_index_k_project.argtypes = [i64, vp, i32, vp, i32, vp, vp, vp, i64, vp, vp]
+    lib.csa2_index_topk_static_capacity.argtypes = [vp]
+    lib.csa2_index_topk_static.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, i64, i32, vp, vp,
+                                           vp, vp]
     lib.csa2_index_topk.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, i64, i32, vp, vp, vp, i64,
                                     vp, vp]
     for name in EXPORTED[1:]:
@@ -101,6 +105,24 @@ def csa2_index_topk(batch, n_heads, head_dim, q_fp4, q_scale, head_w, k_fp4, k_s
                                   _ptr(q_scale), _ptr(head_w), _ptr(k_fp4), _ptr(k_scale),
                                   int(max_len), int(k), _ptr(idx), _ptr(count), _ptr(workspace),
                                   int(workspace_bytes), _ptr(d_err), _stream(stream))
+
+
+def csa2_index_topk_static_capacity() -> int:
+    """Bytes of the fixed scratch array csa2_index_topk_static uses."""
+    out = C.c_int64(0)
+    _check(load().csa2_index_topk_static_capacity(C.byref(out)), "csa2_index_topk_static_capacity")
+    return int(out.value)
+
+
+def csa2_index_topk_static(batch, n_heads, head_dim, q_fp4, q_scale, head_w, k_fp4, k_scale,
+                           max_len, k, idx, count, d_err, stream=None) -> int:
+    """csa2_index_topk with the library's fixed scratch array instead of a
+    workspace (for callers that cannot allocate device memory)."""
+    st, keep = make_batch(batch)
+    return load().csa2_index_topk_static(C.byref(st), int(n_heads), int(head_dim), _ptr(q_fp4),
+                                         _ptr(q_scale), _ptr(head_w), _ptr(k_fp4), _ptr(k_scale),
+                                         int(max_len), int(k), _ptr(idx), _ptr(count),
+                                         _ptr(d_err), _stream(stream))
 
 
 def csa2_index_k_project(n, x_bf16, dim_in, w_bf16, dim_out, dst_row, k_fp4, k_scale, rows,

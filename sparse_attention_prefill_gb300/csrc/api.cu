@@ -11,6 +11,7 @@ extern "C" CSA2_API const char *csa2_status_string(int status) {
     case CSA2_ERR_UNSUPPORTED: return "unsupported configuration";
     case CSA2_ERR_CUDA: return "CUDA launch failure";
     case CSA2_ERR_TIMEOUT: return "timeout";
+    case CSA2_ERR_TOO_LARGE: return "request exceeds the fixed scratch of the allocation-free call";
     default: return "unknown status";
   }
 }
