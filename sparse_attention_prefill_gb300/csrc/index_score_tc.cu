@@ -13,8 +13,11 @@
 // reads its TMEM lane (key j) and sums w[q,h] * ReLU(D[j, (q,h)]) over the
 // head columns of query q.  MXFP4 operands are dequantised to f16 in shared
 // memory: an E2M1 value times a power-of-two scale is exact in f16 (for
-// scales in [2^-23, 2^12]) and f16 products accumulate exactly in fp32, so the
-// per-head dots are exact; only the fp32 head sum rounds.
+// scales in [2^-23, 2^12]), every product is exact, and so is the fp32 sum of
+// one 32-channel group; the sum across the four groups of a 128-channel dot
+// rounds in fp32 when their scales spread it past 24 bits (the tensor core's
+// accumulation order is unspecified), and the head sum rounds.  The scores are
+// held to 1e-5 of sum_h |w_h| ReLU(dot_h).
 //
 // Work unit (one CTA): a tile of 256/Hi consecutive query rows and a chunk of
 // 32 key tiles (4096 keys or pool slots).  Rows of the tile that belong to the
@@ -91,7 +94,6 @@ struct Misc {
   int ident[kMaxQT];         // pool mode: blocks are 0..nb-1
   int cand_smem;             // pool mode: the chunk's candidate blocks are in shared memory
   int cand_span, b_lo;       //   as [query of the tile][block - b_lo]
-  int stride;                // key tiles: every stride-th tile (sample mode), else 1
   float thr[kMaxQT];         // list mode: per-query threshold
   alignas(16) float w[256];  // head weights of the tile, halved
 };
@@ -170,7 +172,9 @@ struct Params {
 };
 
 // key tiles of a row of `len` keys walked by this launch (every stride-th)
-__device__ __forceinline__ int64_t walked_tiles(int64_t len, int stride) {
+template <int STRIDE>
+__device__ __forceinline__ int64_t walked_tiles(int64_t len) {
+  constexpr int stride = STRIDE;
   const int64_t nt = (len + kKeyTile - 1) / kKeyTile;
   return (nt + stride - 1) / stride;
 }
@@ -220,10 +224,11 @@ static_assert(kProdThreads % 4 == 0, "a thread's items share one 32-dim group");
 // run's keys (or, in pool mode, holding no visible entry) read key row 0 and
 // are zeroed when stored: every load is issued unconditionally, so no load
 // waits on another.
+template <int STRIDE>
 __device__ __forceinline__ void load_tile(const Params &P, const Misc *ms, const CandView &cv,
                                           int ri, int64_t kt, int q0, int ptid, KeyLoad &L) {
   const RunInfo ru = ms->runs[ri];
-  const int s0 = (int)kt * ms->stride * kKeyTile;
+  const int s0 = (int)kt * STRIDE * kKeyTile;
   const int lim = (int)(ru.gather ? ru.len : min(ru.len, ru.lim));
   const int64_t nvis = ms->n_vis[ru.ql0];
   L.valid = 0;
@@ -246,10 +251,11 @@ __device__ __forceinline__ void load_tile(const Params &P, const Misc *ms, const
 }
 
 // next (run, tile) after (ri, kt) within key chunk y; false when none is left
+template <int STRIDE>
 __device__ __forceinline__ bool next_item(const Misc *ms, int y, int &ri, int64_t &kt) {
   ++kt;
   while (ri < ms->nruns) {
-    const int64_t nt = walked_tiles(ms->runs[ri].len, ms->stride);
+    const int64_t nt = walked_tiles<STRIDE>(ms->runs[ri].len);
     const int64_t hi = min(nt, (int64_t)(y + 1) * kTilesPerChunk);
     if (kt < hi) return true;
     ++ri;
@@ -258,6 +264,7 @@ __device__ __forceinline__ bool next_item(const Misc *ms, int y, int &ri, int64_
   return false;
 }
 
+template <int STRIDE>
 __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms, int q0, int y) {
   const int ptid = threadIdx.x - kProdWarp0 * 32;
   const int lane = threadIdx.x & 31;
@@ -265,18 +272,18 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
   uint32_t it = 0;
   int ri = 0;
   int64_t kt = (int64_t)y * kTilesPerChunk - 1;
-  if (!next_item(ms, y, ri, kt)) return;
+  if (!next_item<STRIDE>(ms, y, ri, kt)) return;
   KeyLoad ka, kb;
   const CandView cv = cand_view(P, ms, smem);
-  load_tile(P, ms, cv, ri, kt, q0, ptid, ka);
+  load_tile<STRIDE>(P, ms, cv, ri, kt, q0, ptid, ka);
   bool more = true;
   // store the tile held in `use` after issuing the loads of the next tile
   // into `pre` (two fixed buffers: no register copy waits on pending loads)
   auto step = [&](KeyLoad &use, KeyLoad &pre) -> bool {
     int ri2 = ri;
     int64_t kt2 = kt;
-    more = next_item(ms, y, ri2, kt2);
-    if (more) load_tile(P, ms, cv, ri2, kt2, q0, ptid, pre);
+    more = next_item<STRIDE>(ms, y, ri2, kt2);
+    if (more) load_tile<STRIDE>(P, ms, cv, ri2, kt2, q0, ptid, pre);
     const uint32_t st = it % kStages;
     if (!wait_bar(&ms->a_empty[st], ((it / kStages) & 1) ^ 1, ms)) return false;
     uint8_t *A = smem + kOffA + st * kAStage;
@@ -318,6 +325,7 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
   if (lane == 0) raise_err(P.d_err, err);
 }
 
+template <int STRIDE>
 __device__ void mma_role(const Params &P, uint8_t *smem, Misc *ms, int y) {
   const int lane = threadIdx.x & 31;
   if (lane == 0) {
@@ -327,7 +335,7 @@ __device__ void mma_role(const Params &P, uint8_t *smem, Misc *ms, int y) {
     bool ok = true;
     for (int ri = 0; ri < ms->nruns && ok; ++ri) {
       const RunInfo ru = ms->runs[ri];
-      const int64_t nt = walked_tiles(ru.len, ms->stride);
+      const int64_t nt = walked_tiles<STRIDE>(ru.len);
       uint32_t n = (uint32_t)(ru.nq * P.hi);
       n = (n + 15u) & ~15u;
       const uint32_t idesc = make_idesc_f16(128, n, false, false);
@@ -358,7 +366,7 @@ __device__ void mma_role(const Params &P, uint8_t *smem, Misc *ms, int y) {
   __syncwarp();
 }
 
-template <int HI, bool kList>
+template <int HI, bool kList, int STRIDE>
 __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, int y) {
   const CandView cv = cand_view(P, ms, smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -371,14 +379,14 @@ __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
   bool ok = true;
   for (int ri = 0; ri < ms->nruns && ok; ++ri) {
     const RunInfo ru = ms->runs[ri];
-    const int64_t nt = walked_tiles(ru.len, ms->stride);
+    const int64_t nt = walked_tiles<STRIDE>(ru.len);
     for (int64_t kt = (int64_t)y * kTilesPerChunk;
          kt < nt && kt < (int64_t)(y + 1) * kTilesPerChunk; ++kt, ++it) {
       const uint32_t db = it & 1;
       if (!(ok = wait_bar(&ms->d_full[db], (it >> 1) & 1, ms))) break;
       fence_after_sync();
       const int r = 32 * sp + lane;                       // key of the tile
-      const int s = (int)kt * ms->stride * kKeyTile + r;  // its slot in the row
+      const int s = (int)kt * STRIDE * kKeyTile + r;      // its slot in the row
       const int col = (int)kt * kKeyTile + r;             // its column in `scores`
       // w . ReLU(D) over the HI head columns of query ql; store, or append to
       // the query's list (called by the whole warp: the append is
@@ -469,8 +477,12 @@ __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
   }
 }
 
-template <int HI, bool kList>
+// MODE 0: dense score rows; 1: sample (every kStreamStride-th key tile,
+// stored densely); 2: appending lists
+template <int HI, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
+  constexpr int STRIDE = MODE == 1 ? kStreamStride : 1;
+  constexpr bool kList = MODE == 2;
   extern __shared__ __align__(1024) uint8_t smem[];
   Misc *ms = reinterpret_cast<Misc *>(smem + kOffMisc);
   constexpr int QT = 256 / HI;
@@ -527,7 +539,6 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
                                ? P.list_thr[q0 + threadIdx.x] : 0.f;
   if (threadIdx.x == 0) {
     ms->abort = 0;
-    ms->stride = P.stride;
     ms->wait_ns = P.wait_ns;
     ms->cand_smem = 0;
     for (int i = 0; i < kStages; ++i) {
@@ -624,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
   // does this CTA's key chunk hold any work?
   bool any = false;
   for (int ri = 0; ri < ms->nruns; ++ri)
-    any |= walked_tiles(ms->runs[ri].len, ms->stride) > (int64_t)y * kTilesPerChunk;
+    any |= walked_tiles<STRIDE>(ms->runs[ri].len) > (int64_t)y * kTilesPerChunk;
   if (!any) {
     raise_err(P.d_err, err);
     return;
@@ -665,11 +676,11 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
     fence_after_sync();
   }
   if (warp < kEpiWarps) {
-    epilogue_role<HI, kList>(P, smem, ms, q0, y);
+    epilogue_role<HI, kList, STRIDE>(P, smem, ms, q0, y);
   } else if (warp == kMmaWarp) {
-    mma_role(P, smem, ms, y);
+    mma_role<STRIDE>(P, smem, ms, y);
   } else {
-    producer_role(P, smem, ms, q0, y);
+    producer_role<STRIDE>(P, smem, ms, q0, y);
   }
   err = __reduce_or_sync(0xffffffffu, err);
   if ((threadIdx.x & 31) == 0) raise_err(P.d_err, err);
@@ -699,13 +710,17 @@ int launch(Params &P, int n_heads, cudaStream_t st) {
 #define CSA2_LAUNCH(H)                                                                       \
   do {                                                                                       \
     if (P.list_cnt) {                                                                        \
-      cudaFuncSetAttribute(index_score_tc_kernel<H, true>,                                   \
+      cudaFuncSetAttribute(index_score_tc_kernel<H, 2>,                                      \
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);    \
-      index_score_tc_kernel<H, true><<<grid, kThreads, kSmemBytes, st>>>(P);                 \
+      index_score_tc_kernel<H, 2><<<grid, kThreads, kSmemBytes, st>>>(P);                    \
+    } else if (P.stride != 1) {                                                              \
+      cudaFuncSetAttribute(index_score_tc_kernel<H, 1>,                                      \
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);    \
+      index_score_tc_kernel<H, 1><<<grid, kThreads, kSmemBytes, st>>>(P);                    \
     } else {                                                                                 \
-      cudaFuncSetAttribute(index_score_tc_kernel<H, false>,                                  \
+      cudaFuncSetAttribute(index_score_tc_kernel<H, 0>,                                      \
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);    \
-      index_score_tc_kernel<H, false><<<grid, kThreads, kSmemBytes, st>>>(P);                \
+      index_score_tc_kernel<H, 0><<<grid, kThreads, kSmemBytes, st>>>(P);                    \
     }                                                                                        \
   } while (0)
   switch (n_heads) {
@@ -768,6 +783,7 @@ int index_score_sample(const Batch &b, int n_heads, const uint8_t *q_fp4, const 
   Params P;
   if (!base_params(P, b, n_heads, q_fp4, q_scale, head_w, k_fp4, k_scale, max_len, d_err))
     return CSA2_ERR_UNSUPPORTED;
+  if (stride != kStreamStride) return CSA2_ERR_UNSUPPORTED;   // the sample kernel's stride
   P.stride = stride;
   P.scores = sample;
   P.out_ld = sample_ld;

@@ -129,6 +129,7 @@ __device__ uint32_t select_topk(const Keys &keys, int64_t n, uint32_t k, SelectS
   // is kept) selects nothing; the radix search below assumes k >= 1, since
   // with k = 0 no bin would ever hold the k-th key and the threshold would
   // stay at 0.  k is uniform over the block, so every thread returns here.
+  static_assert(NT >= 256, "one thread per histogram bin in the scan below");
   if (k == 0u) return 0u;
   // radix select of the k-th largest key; the first pass also counts the
   // eligible keys (the histogram total)
@@ -758,6 +759,38 @@ topk_kernel(Batch b, const float *__restrict__ scores, int64_t ld, int k,
   if (threadIdx.x == 0) raise_err(d_err, err);
 }
 
+// Full-visible rows of moderate length (4097 to 16384 keys) with CTAs that
+// hold no row in registers (45 registers, 35 KB of shared memory: six rows in
+// flight per SM instead of two): the row is read twice from L2/HBM, once for
+// the strided sample that sets the threshold guess and once to list the keys
+// at or above it, and the exact search runs on the list (the same selection
+// as the long-row path).  A guess that misses falls back to the 4-pass radix
+// select over the row.
+template <int NT>
+__global__ void __launch_bounds__(NT)
+topk_list_kernel(Batch b, const float *__restrict__ scores, int64_t ld, int k,
+                 int32_t *__restrict__ idx, int32_t *__restrict__ count,
+                 int32_t *__restrict__ d_err) {
+  __shared__ SelectShared<NT> sh;
+  __shared__ RegShared<NT> rsh;
+  const int q = blockIdx.x;
+  int err = 0;
+  int64_t n_vis, row_len;
+  row_geometry(b, q, nullptr, 1, 1, ld, nullptr, n_vis, row_len, err, sh);
+  RowView view{scores + (int64_t)q * ld, nullptr, 1, n_vis};
+  int32_t *out = idx + (int64_t)q * k;
+  auto emit = [&](int64_t s, uint32_t slot) { out[slot] = (int32_t)s; };
+  uint32_t got;
+  if (select_topk_listed<NT>(view, row_len, (uint32_t)k, rsh, emit))
+    got = (uint32_t)k;
+  else
+    got = select_topk<NT>(view, row_len, (uint32_t)k, sh, emit);
+  for (int i = (int)got + threadIdx.x; i < k; i += NT) out[i] = -1;
+  if (threadIdx.x == 0) count[q] = (int32_t)got;
+  err = __reduce_or_sync(0xffffffffu, err);
+  if ((threadIdx.x & 31) == 0) raise_err(d_err, err);
+}
+
 __global__ void __launch_bounds__(kThreads)
 candidate_blocks_kernel(Batch b, const float *__restrict__ scores, int64_t ld, int block,
                         int max_blocks, int32_t *__restrict__ blocks,
@@ -1139,7 +1172,9 @@ int topk_launch(const Batch &b, const float *scores, int64_t ld, int k,
     kern<<<b.num_q, nt, smem, st>>>(b, scores, ld, k, cand_blocks, block, max_blocks, idx, count,
                                     d_err, staged);
   };
-  if (row_cap <= 256 * 4) launch(topk_kernel<256, 4>, 256, 0, 0);
+  if (!cand_blocks && row_cap > 4096 && row_cap <= 256 * 64) {
+    topk_list_kernel<256><<<b.num_q, 256, 0, st>>>(b, scores, ld, k, idx, count, d_err);
+  } else if (row_cap <= 256 * 4) launch(topk_kernel<256, 4>, 256, 0, 0);
   else if (row_cap <= 256 * 8) launch(topk_kernel<256, 8>, 256, 0, 0);
   else if (row_cap <= 256 * 16) launch(topk_kernel<256, 16>, 256, 0, 0);
   else if (row_cap <= 256 * 32) launch(topk_kernel<256, 32>, 256, 0, 0);
