@@ -331,7 +331,10 @@ __device__ __forceinline__ void load_step(const int *list, const Src &S, int row
 // column block, whose 16-byte chunk positions repeat the first block's, so
 // they store their upper half first and every phase touches 8 distinct
 // positions.  Rows at or past `valid_rows` (step-relative) are written as zeros.
-template <bool kMasked, bool kFp4>
+// kKind: 0 every row FP8, 1 every row FP4 (selected rows of the FP4 layout),
+// 2 rows below fp4_rows FP4 and the rest FP8 (a step that crosses from the
+// selected rows into the window)
+template <bool kMasked, int kKind>
 __device__ __forceinline__ void store_step(uint8_t *R, int half, bool swap, int row0,
                                            const uint32_t (&off)[kItemsPerThread][2],
                                            int64_t valid_rows, int64_t fp4_rows,
@@ -348,7 +351,7 @@ __device__ __forceinline__ void store_step(uint8_t *R, int half, bool swap, int 
       }
       uint32_t h[8];
       __half2 s2;
-      if (kFp4 && row0 + i * kRowStride < fp4_rows) {
+      if (kKind == 1 || (kKind == 2 && row0 + i * kRowStride < fp4_rows)) {
         // E2M1 x E4M3 scale is exact in f16 (at most 5 significant bits,
         // magnitudes in [2^-10, 2688])
         uint32_t sl, sh;
@@ -487,18 +490,28 @@ __device__ void producer_role(const Params &P, const CUtensorMap *tmap_q, uint8_
       uint8_t *R = smem + kOffR + buf * kRBuf;
       const int64_t valid_rows = S.nrows - (int64_t)st * kStepRows;
       const int64_t fp4_rows = S.nsel - (int64_t)st * kStepRows;
-      if (valid_rows >= kStepRows)
-        store_step<false, kFp4>(R, st & 1, swap, row0, off, valid_rows, fp4_rows, use);
-      else
-        store_step<true, kFp4>(R, st & 1, swap, row0, off, valid_rows, fp4_rows, use);
+      if (!kFp4 || fp4_rows <= 0) {             // FP8 rows only
+        if (valid_rows >= kStepRows)
+          store_step<false, 0>(R, st & 1, swap, row0, off, valid_rows, fp4_rows, use);
+        else
+          store_step<true, 0>(R, st & 1, swap, row0, off, valid_rows, fp4_rows, use);
+      } else if (fp4_rows >= kStepRows) {      // FP4 rows only (valid_rows >= fp4_rows)
+        store_step<false, 1>(R, st & 1, swap, row0, off, valid_rows, fp4_rows, use);
+      } else {
+        store_step<true, 2>(R, st & 1, swap, row0, off, valid_rows, fp4_rows, use);
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ms->r_full[buf]);
       return true;
     };
-    for (int st = 0; st < nsteps && ok; st += 2) {
+    // one copy of the step body: the prefetched items move into place at the
+    // end of a step (their loads have had the whole store to land)
+#pragma unroll 1
+    for (int st = 0; st < nsteps && ok; ++st) {
       ok = step(st, b0, b1);
-      if (ok && st + 1 < nsteps) ok = step(st + 1, b1, b0);
+#pragma unroll
+      for (int i = 0; i < kItemsPerThread; ++i) b0[i] = b1[i];
     }
     g += nch;
     if (!ok) break;
