@@ -25,8 +25,10 @@
 //
 // Roles (16 warps, one CTA per SM, persistent over queries):
 //   warps 0-7   softmax + epilogue; warp w reads TMEM sub-partition w%4 and
-//               heads 32*(w/4) .. +31 (rows of S^T, channels of O^T); warp 0
-//               also builds the next query's row list one query ahead
+//               heads 32*(w/4) .. +31 (rows of S^T, channels of O^T); S^T is
+//               read 16 lanes wide (its M = 64 rows fill lanes 0-15 of each
+//               sub-partition), so every thread holds two rows x 8 heads;
+//               warp 0 also builds the next query's row list one query ahead
 //   warp 8      TMEM allocation; lane 0 issues the S^T MMAs
 //   warp 9      lane 0 issues the O^T MMAs (the two products of neighbouring
 //               chunks are issued independently, so neither waits behind the
@@ -35,8 +37,9 @@
 //               in 128-byte swizzle, converted bf16 -> f16 in place), row
 //               gather + E4M3 -> f16 dequant in steps of 32 rows, loads issued
 //               one step ahead; a chunk buffer is released in 32-row halves
-// The per-query row sums and maxima are reduced across a warp's lanes with a
-// reduce-scatter (five halving steps).
+// The per-head row sums and maxima are reduced over the 8 threads holding a
+// head's columns (three butterfly steps), then across the 4 warps of a head
+// half through shared memory.
 // Every wait is bounded (two seconds unless csa2_set_wait_limit_ns says
 // otherwise); on expiry the kernel raises CSA2_DERR_TIMEOUT, drains its MMAs
 // and any Q copy in flight (each for at most two seconds), frees TMEM and
@@ -96,7 +99,7 @@ struct Misc {
   uint32_t tmem_base;
   int abort;
   int votes[2][8];      // softmax warps: "a logit exceeded the reference", by chunk parity
-  float m_ref[64];      // reference maximum per head (log2 units)
+  alignas(16) float m_ref[64];   // reference maximum per head (log2 units)
   float alpha[64];      // rescale factors of the current slow path
   float red[4][64];     // cross-warp reductions
 };
@@ -641,24 +644,6 @@ __device__ void o_issuer_role(const Params &P, uint8_t *smem, Misc *ms) {
 // ---------------------------------------------------------------------------
 // softmax + epilogue (warps 0-7)
 // ---------------------------------------------------------------------------
-// Reduce 32 per-lane values across the warp so that lane j ends with the
-// reduction of value j over all lanes: five halving steps, each lane keeping
-// the half of the values whose index bit matches its lane bit.  v is consumed.
-template <class Op>
-__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane, Op op) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    const bool upper = (lane & o) != 0;
-#pragma unroll
-    for (int i = 0; i < o; ++i) {
-      const float send = upper ? v[i] : v[i + o];
-      const float keep = upper ? v[i + o] : v[i];
-      v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, o));
-    }
-  }
-  return v[0];
-}
-
 __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sp = warp & 3;          // TMEM sub-partition: lanes 32*sp ..
@@ -667,7 +652,7 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
   const uint32_t tmem = ms->tmem_base;
   const uint32_t lane_addr = (uint32_t)(32 * sp) << 16;
   const float NEG_INF = -INFINITY;
-  float lsum[32];
+  float lsum[8];   // this thread's heads 32hh + 8k + hc + e, as [2k + e]
   uint32_t g = 0, qi = 0, gp = 0;
   bool ok = true;
   int err = 0;
@@ -700,27 +685,39 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
     const int nch = n_chunks_of(nrows);
     publish(q + gridDim.x, qi + 1);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) lsum[j] = 0.f;
+    for (int j = 0; j < 8; ++j) lsum[j] = 0.f;
     for (int c = 0; c < nch; ++c, ++g) {
       const uint32_t sb = g & 1, ph = (g >> 1) & 1;
       ok = wait_bar(&ms->s_full[sb], ph, ms);
       if (!ok) break;
       fence_after_sync();
-      uint32_t v[32];
-      tmem_ld32x32b_x32(tmem + lane_addr + kColS + sb * 64 + 32 * hh, v);
+      uint32_t v[16];
+      tmem_ld16x256b_x4(tmem + lane_addr + kColS + sb * 64 + 32 * hh, v);
       tmem_wait_ld();
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ms->s_empty[sb]);
-      // M = 64 layout: lanes 0-15 of this sub-partition hold rows 16*sp + lane
-      const int crow = 16 * sp + lane;
-      const bool valid = lane < 16 && (int64_t)c * kChunk + crow < nrows;
-      float x[32];
+      // M = 64 layout, read 16 lanes wide: this thread holds chunk rows crow
+      // and crow + 8 (lanes t/4 and t/4 + 8 of the sub-partition) and the
+      // column pairs 8k + hc, +1 (k < 4) of the warp's 32 heads:
+      // v[4k + 2r + e] = row crow + 8r, head 32hh + 8k + hc + e
+      const int crow = 16 * sp + (lane >> 2);
+      const int hc = 2 * (lane & 3);
+      const bool valid0 = (int64_t)c * kChunk + crow < nrows;
+      const bool valid1 = (int64_t)c * kChunk + crow + 8 < nrows;
+      float x[16], mr[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 m2 = *reinterpret_cast<const float2 *>(&ms->m_ref[32 * hh + 8 * k + hc]);
+        mr[2 * k] = m2.x;
+        mr[2 * k + 1] = m2.y;
+      }
       bool exceed = false;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        x[j] = valid ? __uint_as_float(v[j]) * P.scale_log2 : NEG_INF;
-        exceed |= x[j] > ms->m_ref[32 * hh + j] + 8.f;
+      for (int i = 0; i < 16; ++i) {
+        const bool vr = (i & 2) ? valid1 : valid0;
+        x[i] = vr ? __uint_as_float(v[i]) * P.scale_log2 : NEG_INF;
+        exceed |= x[i] > mr[2 * (i >> 2) + (i & 1)] + 8.f;
       }
       // does any logit of the chunk exceed its head's reference by 2^8?
       const int vb = g & 1;
@@ -731,13 +728,27 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
 #pragma unroll
       for (int w = 0; w < kSoftmaxWarps; ++w) slow |= ms->votes[vb][w] != 0;
       if (slow) {
-        // per-head maximum over the warp's rows (butterfly per head), then
-        // across the 4 warps of this head half
-        float xm[32];
+        // per-head maximum: over this thread's two rows, then over the 8
+        // threads holding the same columns, then across the 4 warps of this
+        // head half
+        float hm[8];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) xm[j] = x[j];
-        const float mine = reduce_scatter32(xm, lane, [](float a, float b) { return fmaxf(a, b); });
-        ms->red[sp][32 * hh + lane] = mine;
+        for (int k = 0; k < 4; ++k) {
+          hm[2 * k] = fmaxf(x[4 * k], x[4 * k + 2]);
+          hm[2 * k + 1] = fmaxf(x[4 * k + 1], x[4 * k + 3]);
+        }
+#pragma unroll
+        for (int o = 4; o <= 16; o <<= 1) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) hm[j] = fmaxf(hm[j], __shfl_xor_sync(0xffffffffu, hm[j], o));
+        }
+        if (lane < 4) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            ms->red[sp][32 * hh + 8 * k + hc] = hm[2 * k];
+            ms->red[sp][32 * hh + 8 * k + hc + 1] = hm[2 * k + 1];
+          }
+        }
         if (!(ok = group_sync(&ms->sm_grp, gp, ms))) break;
         if (stid < 64) {
           const float old = ms->m_ref[stid];
@@ -749,7 +760,12 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
         }
         if (!(ok = group_sync(&ms->sm_grp, gp, ms))) break;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) lsum[j] *= ms->alpha[32 * hh + j];
+        for (int k = 0; k < 4; ++k) {
+          lsum[2 * k] *= ms->alpha[32 * hh + 8 * k + hc];
+          lsum[2 * k + 1] *= ms->alpha[32 * hh + 8 * k + hc + 1];
+          mr[2 * k] = ms->m_ref[32 * hh + 8 * k + hc];
+          mr[2 * k + 1] = ms->m_ref[32 * hh + 8 * k + hc + 1];
+        }
         if (c > 0) {
           // every earlier O^T MMA of this query must be complete: the latest
           // one issued is O^T(g-1)
@@ -774,23 +790,21 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
       // P(g) goes to buffer g&1 once O^T(g-2) has consumed it
       ok = wait_bar(&ms->p_empty[sb], ph ^ 1, ms);
       if (!ok) break;
-      uint32_t pk[16];
+      uint8_t *Pb = smem + kOffP + sb * kPBuf;
 #pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        const float m0 = ms->m_ref[32 * hh + j], m1 = ms->m_ref[32 * hh + j + 1];
-        const float p0 = ex2(x[j] - (m0 == NEG_INF ? 0.f : m0));
-        const float p1 = ex2(x[j + 1] - (m1 == NEG_INF ? 0.f : m1));
-        lsum[j] += p0;
-        lsum[j + 1] += p1;
-        __half2 h2 = __floats2half2_rn(p0, p1);
-        pk[j / 2] = *reinterpret_cast<uint32_t *>(&h2);
-      }
-      if (lane < 16) {
-        uint8_t *Pb = smem + kOffP + sb * kPBuf;
+      for (int k = 0; k < 4; ++k) {
+        const float m0 = mr[2 * k] == NEG_INF ? 0.f : mr[2 * k];
+        const float m1 = mr[2 * k + 1] == NEG_INF ? 0.f : mr[2 * k + 1];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          *reinterpret_cast<uint4 *>(Pb + sw128_offset(crow, 32 * hh + 8 * i, 0)) =
-              make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        for (int r = 0; r < 2; ++r) {
+          const float p0 = ex2(x[4 * k + 2 * r] - m0);
+          const float p1 = ex2(x[4 * k + 2 * r + 1] - m1);
+          lsum[2 * k] += p0;
+          lsum[2 * k + 1] += p1;
+          __half2 h2 = __floats2half2_rn(p0, p1);
+          *reinterpret_cast<uint32_t *>(Pb + sw128_offset(crow + 8 * r, 32 * hh + 8 * k + hc, 0)) =
+              *reinterpret_cast<uint32_t *>(&h2);
+        }
       }
       fence_proxy_async_smem();
       fence_before_sync();
@@ -799,9 +813,22 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
     }
     if (!ok) break;
     // ---- epilogue: row sums, normalisation, bf16 output, lse
-    // lane j: the warp's sum of lsum[j] (recursive halving: 31 shuffles)
-    const float lmine = reduce_scatter32(lsum, lane, [](float a, float b) { return a + b; });
-    ms->red[sp][32 * hh + lane] = lmine;
+    // per head: over the 8 threads holding its columns, then across the warps
+    {
+      const int hc = 2 * (lane & 3);
+#pragma unroll
+      for (int o = 4; o <= 16; o <<= 1) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) lsum[j] += __shfl_xor_sync(0xffffffffu, lsum[j], o);
+      }
+      if (lane < 4) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          ms->red[sp][32 * hh + 8 * k + hc] = lsum[2 * k];
+          ms->red[sp][32 * hh + 8 * k + hc + 1] = lsum[2 * k + 1];
+        }
+      }
+    }
     if (!(ok = group_sync(&ms->sm_grp, gp, ms))) break;
     if (stid < 64) {
       float l = (ms->red[0][stid] + ms->red[1][stid]) + (ms->red[2][stid] + ms->red[3][stid]);

@@ -206,6 +206,20 @@ __device__ __forceinline__ void tmem_ld32x32b_x16(uint32_t taddr, uint32_t (&r)[
       : "r"(taddr));
 }
 
+// 16 lanes x 256 bits, four repetitions: thread t holds lanes t/4 and t/4 + 8
+// of the warp's sub-partition, columns 8k + 2(t%4) and +1 of repetition k:
+// r[4k + 2*(second lane) + (second column)].  Suits an M = 64 accumulator,
+// whose rows fill lanes 0-15 of each sub-partition.
+__device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_ld32x32b_x8(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
