@@ -60,7 +60,81 @@ def parse():
                     help="skip the decoder-tail block measurement (c2_decoder_replay)")
     ap.add_argument("--configs", action="store_true",
                     help="instead of the bench line: layer-queries/s of each of the five workloads")
+    ap.add_argument("--profile", choices=PROFILE_TARGETS, default=None,
+                    help="instead of the bench line: run --steps passes of one call sequence, L2 "
+                         "flushed before each, and nothing else (a fixed launch sequence for ncu)")
     return ap.parse_args()
+
+
+PROFILE_TARGETS = ("c2_decoder_replay", "c3_encoder_prefill", "c3_streamed", "c2_fp4kv",
+                   "index_k_project")
+
+
+def run_profile(args):
+    """--steps passes of one call sequence (L2 flushed before each pass), for
+    ncu launch lists and captures:
+      c2_decoder_replay   the decoder-tail step (9 launches per pass)
+      c3_encoder_prefill  the encoder-prefill Full layer (index score, top-K, attention)
+      c3_streamed         its streamed score -> top-K (5 launches per pass)
+      c2_fp4kv            one decoder-tail step, then per pass the L22 attention over the FP8
+                          pool and over the FP4 main-KV copy of it (2 launches per pass)
+      index_k_project     the index-K projection of 65,536 entries"""
+    import torch
+    import sparse_attention_prefill_gb300 as S
+    from sparse_attention_prefill_gb300 import synth
+    from sparse_attention_prefill_gb300.layer import LayerRunner
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    S.load()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    d_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    name = args.profile
+    if name == "index_k_project":
+        n = 65536
+        g = torch.Generator(device=dev).manual_seed(args.seed + 17)
+        x = torch.randn((n, 512), generator=g, device=dev).to(torch.bfloat16)
+        wt = (torch.randn((128, 512), generator=g, device=dev) / 512 ** 0.5).to(torch.bfloat16)
+        dst = torch.arange(n, dtype=torch.int64, device=dev)
+        codes = torch.empty((n, 64), dtype=torch.uint8, device=dev)
+        scales = torch.empty((n, 4), dtype=torch.float32, device=dev)
+        fn = lambda: S.index_k_project(x, wt, dst, codes, scales, d_err=d_err)   # noqa: E731
+    else:
+        wname = "c2_decoder_replay" if name.startswith("c2") else "c3_encoder_prefill"
+        w = synth.config(wname, dev, args.seed)
+        run = LayerRunner(w)
+        d_err = run.d_err
+        if name == "c2_decoder_replay":
+            fn = run.decoder_tail_step
+        elif name == "c3_encoder_prefill":
+            fn = lambda: run.full_layer("full")   # noqa: E731
+        elif name == "c3_streamed":
+            b, L = run.batches["full"], w.layers["full"]
+            ws = torch.empty(S.csa2_index_topk_workspace(run.nq, w.ld), dtype=torch.uint8,
+                             device=dev)
+            fn = lambda: S.index_topk(b, L.q_fp4, L.q_scale, L.head_w, w.pool.k_fp4,   # noqa: E731
+                                      w.pool.k_scale, w.ld, w.topk, idx=run.idx["full"],
+                                      count=run.count["full"], workspace=ws, d_err=d_err)
+        else:
+            run.decoder_tail_step()
+            synth.with_fp4kv(w, args.seed)
+            L = w.layers["L22"]
+            q, idx, b = run._lt("L22", "q"), run.idx["L21"], run.batches["L22"]
+
+            def fn():
+                S.sparse_swa_attn(b, q, w.pool.kv_fp8, w.pool.kv_scale, idx, L.swa_fp8,
+                                  L.swa_scale, run.tail_win_lo, w.window, w.sm_scale,
+                                  out=run.out["L22"], lse=run.lse["L22"], d_err=d_err)
+                flush.zero_()
+                S.sparse_swa_attn_fp4kv(b, q, w.pool.kv_fp4, w.pool.kv_sf, idx, L.swa_fp8,
+                                        L.swa_scale, run.tail_win_lo, w.window, w.sm_scale,
+                                        out=run.out["L22"], lse=run.lse["L22"], d_err=d_err)
+    for _ in range(args.steps):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    assert int(d_err.item()) == 0, "device data-error flags raised"
+    print("profile run done: %s x %d" % (name, args.steps))
+    return 0
 
 
 def dist_env():
@@ -1109,6 +1183,8 @@ def main():
 
     if args.configs:
         return bench_configs(args) if rank == 0 else 0
+    if args.profile:
+        return run_profile(args) if rank == 0 else 0
     import torch
     if world > 1:
         torch.distributed.init_process_group("nccl")

@@ -11,7 +11,9 @@
 // A CTA takes 128 source rows: D[i, o] (M = 128 rows, N = 128 outputs, K =
 // 512) by tcgen05 kind::f16 with bf16 operands, fp32 accumulation in TMEM.
 // The x and W blocks of 64 channels arrive by TMA (2-D tensor maps, 128-byte
-// swizzle) into a 4-stage ring; one thread issues the loads, one the MMAs.
+// swizzle) into a 2-stage ring (three CTAs share an SM, so that the loads of
+// one overlap the others' MMAs and encoding); one thread issues the loads,
+// one the MMAs.
 // Each of the 128 threads then owns one row: it reads its 128 fp32 values
 // from TMEM and encodes them exactly as csa2_quantize_rows' MXFP4 format does
 // (group scale 2^(floor(log2 amax) - 2) in fp32, x / scale in fp32, E2M1 round
@@ -33,10 +35,10 @@ constexpr int kOut = 128;             // output channels (MMA N)
 constexpr int kIn = 512;              // input channels (MMA K)
 constexpr int kKBlock = 64;           // channels per TMA box (128 bytes of bf16)
 constexpr int kKBlocks = kIn / kKBlock;
-constexpr int kStages = 4;
+constexpr int kStages = 2;            // 64 KB of shared memory: three CTAs per SM
 constexpr uint32_t kTile = kRows * 128;            // 16 KB per operand block
 constexpr uint32_t kStage = 2 * kTile;             // x block + W block
-constexpr uint32_t kOffBar = kStages * kStage;     // 128 KB
+constexpr uint32_t kOffBar = kStages * kStage;     // 64 KB
 constexpr uint32_t kSmem = kOffBar + 256;
 constexpr uint64_t kDrainNs = 2000000000ull;
 
