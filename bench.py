@@ -66,8 +66,8 @@ def parse():
     return ap.parse_args()
 
 
-PROFILE_TARGETS = ("c2_decoder_replay", "c3_encoder_prefill", "c3_streamed", "c2_fp4kv",
-                   "index_k_project")
+PROFILE_TARGETS = ("c2_decoder_replay", "c3_encoder_prefill", "c3_streamed", "c3_long_rows",
+                   "c2_fp4kv", "index_k_project")
 
 
 def run_profile(args):
@@ -76,6 +76,9 @@ def run_profile(args):
       c2_decoder_replay   the decoder-tail step (9 launches per pass)
       c3_encoder_prefill  the encoder-prefill Full layer (index score, top-K, attention)
       c3_streamed         its streamed score -> top-K (5 launches per pass)
+      c3_long_rows        the same Full layer at 2048 of its query rows (every 4th of the last
+                          8192: 12288 to 16384 visible entries each), a small case of the
+                          headline's three kernels for multi-pass captures
       c2_fp4kv            one decoder-tail step, then per pass the L22 attention over the FP8
                           pool and over the FP4 main-KV copy of it (2 launches per pass)
       index_k_project     the index-K projection of 65,536 entries"""
@@ -99,13 +102,17 @@ def run_profile(args):
         scales = torch.empty((n, 4), dtype=torch.float32, device=dev)
         fn = lambda: S.index_k_project(x, wt, dst, codes, scales, d_err=d_err)   # noqa: E731
     else:
-        wname = "c2_decoder_replay" if name.startswith("c2") else "c3_encoder_prefill"
-        w = synth.config(wname, dev, args.seed)
+        if name == "c3_long_rows":
+            w = synth.full_layer(32768, 2, list(range(24576, 32768, 4)), 64, 32, args.seed, dev,
+                                 tag=name)
+        else:
+            wname = "c2_decoder_replay" if name.startswith("c2") else "c3_encoder_prefill"
+            w = synth.config(wname, dev, args.seed)
         run = LayerRunner(w)
         d_err = run.d_err
         if name == "c2_decoder_replay":
             fn = run.decoder_tail_step
-        elif name == "c3_encoder_prefill":
+        elif name in ("c3_encoder_prefill", "c3_long_rows"):
             fn = lambda: run.full_layer("full")   # noqa: E731
         elif name == "c3_streamed":
             b, L = run.batches["full"], w.layers["full"]
