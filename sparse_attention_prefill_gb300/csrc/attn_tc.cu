@@ -851,11 +851,15 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
       tmem_ld32x32b_x32(tmem + lane_addr + kColO + t * 64 + 32 * hh, o);
       tmem_wait_ld();
       const int d = t * 128 + 32 * sp + lane;
+      // two heads per conversion (one cvt.rn.bf16x2.f32), stored apart
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
+      for (int j = 0; j < 32; j += 2) {
         const int h = 32 * hh + j;
-        if (h < P.n_heads)
-          og[(int64_t)h * kDim + d] = __float2bfloat16_rn(__uint_as_float(o[j]) * ms->alpha[h]);
+        const float2 a2 = *reinterpret_cast<const float2 *>(&ms->alpha[h]);
+        const __nv_bfloat162 b2 =
+            __floats2bfloat162_rn(__uint_as_float(o[j]) * a2.x, __uint_as_float(o[j + 1]) * a2.y);
+        if (h < P.n_heads) og[(int64_t)h * kDim + d] = b2.x;
+        if (h + 1 < P.n_heads) og[(int64_t)(h + 1) * kDim + d] = b2.y;
       }
     }
     fence_before_sync();
