@@ -493,6 +493,19 @@ struct SmemKeys {
   __device__ __forceinline__ uint32_t key(int64_t, uint32_t r) const { return r; }
 };
 
+// Score rows read straight from memory take the vectorised listing sweep
+// when they have no candidate blocks.
+template <class Keys>
+constexpr bool kPlainRows = false;
+template <>
+constexpr bool kPlainRows<RowView> = true;
+template <class Keys>
+__device__ __forceinline__ bool plain_rows_cand(const Keys &) { return true; }
+template <>
+__device__ __forceinline__ bool plain_rows_cand<RowView>(const RowView &k) {
+  return k.cand != nullptr;
+}
+
 // Block view: key of block b = max key over its visible entries, plus one, so
 // every block is eligible (the pool is a budget, filled whatever the scores).
 struct BlockView {
@@ -604,6 +617,79 @@ __device__ void select_listed(int n_list, uint32_t mn, uint32_t mx, uint32_t k,
   __syncthreads();
 }
 
+// Listing sweep over a plain score row (no candidate blocks): every score
+// f >= g is appended (its key and position) to the shared list, the counter
+// running on past the capacity.  Equivalent to comparing keys with
+// score_key(g) when that key is nonzero: the key map is monotone, -0 and +0
+// compare equal both ways, and NaN and -inf fail the float comparison.  The
+// row is read 16 bytes per load, four loads per thread in flight; a thread's
+// takes are placed by one warp scan per 16 scores.  Returns this thread's
+// largest listed key (0 if none).
+template <int NT>
+__device__ uint32_t list_row_fast(const float *__restrict__ row, int64_t n, float g,
+                                  RegShared<NT> &sh) {
+  const int t = threadIdx.x, lane = t & 31;
+  uint32_t mx = 0;
+  auto put = [&](uint32_t slot, float f, int64_t i) {
+    const uint32_t x = score_key(f);
+    if (slot < (uint32_t)kListCap) {
+      sh.list_key[slot] = x;
+      sh.list_pos[slot] = (int32_t)i;
+    }
+    mx = max(mx, x);
+  };
+  // scalar edges: the scores before the first 16-byte boundary and after the
+  // last whole vector (at most three each; the row is 4-byte aligned)
+  const int64_t head0 = (int64_t)(((16u - ((uint32_t)(uintptr_t)row & 15u)) & 15u) >> 2);
+  const int64_t head = head0 < n ? head0 : n;
+  const int64_t nvec = (n - head) >> 2;
+  const int64_t tail0 = head + 4 * nvec;
+  if (t < 32) {
+    const int64_t i = lane < head ? (int64_t)lane : tail0 + (lane - head);
+    const bool in = lane < head || (lane >= head && i < n && lane - head < 3);
+    const float f = in ? __ldg(row + i) : 0.f;
+    const bool take = in && f >= g;
+    const uint32_t slot = warp_reserve(take, &sh.out_count);
+    if (take) put(slot, f, i);
+  }
+  const float4 *v4 = reinterpret_cast<const float4 *>(row + head);
+  constexpr int kV = 4;
+  for (int64_t j0 = 0; j0 < nvec; j0 += (int64_t)NT * kV) {
+    float4 v[kV];
+#pragma unroll
+    for (int u = 0; u < kV; ++u) {
+      const int64_t j = j0 + u * NT + t;
+      v[u] = j < nvec ? __ldg(v4 + j) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+    uint32_t c = 0;
+#pragma unroll
+    for (int u = 0; u < kV; ++u)
+      c += (uint32_t)(v[u].x >= g) + (uint32_t)(v[u].y >= g) + (uint32_t)(v[u].z >= g) +
+           (uint32_t)(v[u].w >= g);
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+    if (tot == 0u) continue;
+    uint32_t base = 0;
+    if (lane == 31) base = atomicAdd(&sh.out_count, tot);
+    uint32_t slot = __shfl_sync(0xffffffffu, base, 31) + incl - c;
+    if (c == 0u) continue;
+#pragma unroll
+    for (int u = 0; u < kV; ++u) {
+      const int64_t i = head + 4 * (j0 + u * NT + t);
+      if (v[u].x >= g) put(slot++, v[u].x, i);
+      if (v[u].y >= g) put(slot++, v[u].y, i + 1);
+      if (v[u].z >= g) put(slot++, v[u].z, i + 2);
+      if (v[u].w >= g) put(slot++, v[u].w, i + 3);
+    }
+  }
+  return mx;
+}
+
 // Long rows (past the register path): a threshold guess from the moments of
 // every 16th key, then one sweep that lists the keys at or above it (up to
 // kListCap, with their positions).  With between k and kListCap keys listed
@@ -666,19 +752,25 @@ __device__ bool select_topk_listed(const Keys &keys, int64_t n, uint32_t k, RegS
   const float sd = sqrtf(fmaxf(f_sq / (float)f_cnt - mean * mean, 0.f));
   const float p = (float)(2u * k + 64u) / n_elig;
   if (!(p < 1.f) || !(sd > 0.f)) return false;
-  const uint32_t t_est = score_key(mean + 1.41421356f * erfcinvf(2.f * p) * sd);
+  const float g = mean + 1.41421356f * erfcinvf(2.f * p) * sd;
+  const uint32_t t_est = score_key(g);
   if (t_est == 0u) return false;
   // list the keys >= t_est; the counter runs on past the capacity
   uint32_t mx = 0;
-  sweep<NT>(keys, n, [&](int64_t i, uint32_t x) {
-    const bool take = x != 0u && x >= t_est;
-    const uint32_t slot = warp_reserve(take, &sh.out_count);
-    if (take && slot < (uint32_t)kListCap) {
-      sh.list_key[slot] = x;
-      sh.list_pos[slot] = (int32_t)i;
-    }
-    mx = max(mx, take ? x : 0u);
-  });
+  if constexpr (kPlainRows<Keys>) {
+    if (keys.cand == nullptr) mx = list_row_fast<NT>(keys.row, n, g, sh);
+  }
+  if (!kPlainRows<Keys> || plain_rows_cand(keys)) {
+    sweep<NT>(keys, n, [&](int64_t i, uint32_t x) {
+      const bool take = x != 0u && x >= t_est;
+      const uint32_t slot = warp_reserve(take, &sh.out_count);
+      if (take && slot < (uint32_t)kListCap) {
+        sh.list_key[slot] = x;
+        sh.list_pos[slot] = (int32_t)i;
+      }
+      mx = max(mx, take ? x : 0u);
+    });
+  }
   mx = __reduce_max_sync(0xffffffffu, mx);
   if (lane == 0) sh.red[2][warp] = mx;
   __syncthreads();
