@@ -420,8 +420,13 @@ def bench_headline(args, rank, world, local_rank):
         for name, key in (("f16", "frac_of_f16_peak"), ("e4m3", "frac_of_fp8_peak"),
                           ("e2m1_mx", "frac_of_fp4_peak")):
             index[key] = round(is_tflops / peaks[name]["tflops"], 4)
+    # top-K algorithmic bytes: every visible score read once, the selected
+    # positions and the counts written
+    tk_bytes = pairs * 4 + run.nq * (w.topk + 1) * 4
+    tk_gbs = tk_bytes / (kern["select"] * 1e-3) / 1e9
     topk = {"kernel": "csa2_topk", "avg_launch_ms": round(kern["select"], 4),
-            "share_of_step": share["select"]}
+            "share_of_step": share["select"], "algorithmic_bytes_per_launch": int(tk_bytes),
+            "achieved_gbs": round(tk_gbs, 1), "frac_of_hbm_peak": round(tk_gbs / hbm, 4)}
     streamed = bench_streamed(args, w, run, stream, flush, dev, world)
     e2e = None
     if not args.no_e2e:
