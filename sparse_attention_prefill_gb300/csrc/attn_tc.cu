@@ -419,6 +419,14 @@ __device__ void producer_role(const Params &P, const CUtensorMap *tmap_q, uint8_
       for (int b = 0; b < kDim / 64; ++b)
         tma_load_3d(Qs + b * kQBlock, tmap_q, b * 64, 0, q, &ms->q_tma);
       tma_pending = (int)(qi & 1);
+      // the next query's Q into L2 now, so that its copy at the next query
+      // boundary reads L2 instead of HBM
+      const int qn = q + (int)gridDim.x;
+      if (qn < P.b.num_q)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                         P.q + (int64_t)qn * P.n_heads * kDim),
+                     "r"((uint32_t)(P.n_heads * kDim * 2))
+                     : "memory");
     }
     // ---- row list and counts of this query (built one query ahead by the
     // first softmax warp)
