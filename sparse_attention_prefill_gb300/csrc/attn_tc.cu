@@ -28,26 +28,28 @@
 //               heads 32*(w/4) .. +31 (rows of S^T, channels of O^T); S^T is
 //               read 16 lanes wide (its M = 64 rows fill lanes 0-15 of each
 //               sub-partition), so every thread holds two rows x 8 heads;
-//               warp 0 also builds the next query's row list one query ahead
+//               between a query's last chunk and its epilogue the eight warps
+//               load the next query's Q (bf16 rows, prefetched into L2 a query
+//               ahead), convert it to f16 and store it into the operand buffer
+//               the query's last S^T MMAs have released, so the next query's
+//               first products overlap this query's epilogue
 //   warp 8      TMEM allocation; lane 0 issues the S^T MMAs
 //   warp 9      lane 0 issues the O^T MMAs (the two products of neighbouring
 //               chunks are issued independently, so neither waits behind the
-//               other in one issuing thread)
-//   warps 10-15 producers: Q by TMA (eight 64 x 64 boxes of a 3-D tensor map
-//               in 128-byte swizzle, converted bf16 -> f16 in place), row
-//               gather + E4M3 -> f16 dequant in steps of 32 rows, loads issued
-//               one step ahead; a chunk buffer is released in 32-row halves
+//               other in one issuing thread); the whole warp builds the next
+//               query's row list one query ahead, while it waits for P
+//   warps 10-15 producers: row gather + E4M3 -> f16 dequant in steps of 32
+//               rows, loads issued one step ahead; a chunk buffer is released
+//               in 32-row halves
 // The per-head row sums and maxima are reduced over the 8 threads holding a
 // head's columns (three butterfly steps), then across the 4 warps of a head
 // half through shared memory.
 // Every wait is bounded (two seconds unless csa2_set_wait_limit_ns says
 // otherwise); on expiry the kernel raises CSA2_DERR_TIMEOUT, drains its MMAs
-// and any Q copy in flight (each for at most two seconds), frees TMEM and
-// returns.
+// (for at most two seconds), frees TMEM and returns.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tcgen05.cuh"
-#include "tma.cuh"
 
 namespace csa2 {
 namespace {
@@ -90,7 +92,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;   // drains (the pipeline waits take
 constexpr int kDerrTimeout = 128;
 
 struct Misc {
-  uint64_t q_full, q_empty, q_tma, o_full, o_empty, done, done_o, sm_grp;
+  uint64_t q_full, q_empty, o_full, o_empty, done, done_o, sm_grp;
   uint64_t r_full[2], r_empty[2][2], s_full[2], s_empty[2], p_full[2], p_empty[2];
   uint64_t meta_full[2];
   int64_t meta[2][4];   // per query (ring of 2): selected rows, window rows, first SWA
@@ -386,8 +388,7 @@ __device__ __forceinline__ void store_step(uint8_t *R, int half, bool swap, int 
 }
 
 template <bool kFp4>
-__device__ void producer_role(const Params &P, const CUtensorMap *tmap_q, uint8_t *smem,
-                              Misc *ms) {
+__device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms) {
   const int ptid = threadIdx.x - kProducerWarp0 * 32;
   const int lane = threadIdx.x & 31;
   const int row0 = ptid >> 5, seg = lane;
@@ -401,35 +402,12 @@ __device__ void producer_role(const Params &P, const CUtensorMap *tmap_q, uint8_
     off[i][0] = swap ? hi : lo;
     off[i][1] = swap ? lo : hi;
   }
-  uint8_t *Qs = smem + kOffQ;
   const int *lists = reinterpret_cast<const int *>(smem + kOffList);
   uint32_t g = 0;  // chunks produced by this CTA
   uint32_t qi = 0;
-  // the Q copy last issued by this thread and not yet seen complete (its
-  // phase parity), or -1: it must land before the CTA exits
-  int tma_pending = -1;
   for (int q = blockIdx.x; q < P.b.num_q; q += gridDim.x, ++qi) {
-    // ---- Q of this query: eight 64 x 64 bf16 boxes by TMA, landing in the
-    // SW128 layout (heads past n_heads are the map's zero fill); converted to
-    // f16 in place below (f16 and bf16 are both 2 bytes)
-    if (!wait_bar(&ms->q_empty, (qi & 1) ^ 1, ms)) break;
-    if (ptid == 0) {
-      mbar_arrive_expect_tx(&ms->q_tma, kHeadsPad * kDim * 2);
-#pragma unroll
-      for (int b = 0; b < kDim / 64; ++b)
-        tma_load_3d(Qs + b * kQBlock, tmap_q, b * 64, 0, q, &ms->q_tma);
-      tma_pending = (int)(qi & 1);
-      // the next query's Q into L2 now, so that its copy at the next query
-      // boundary reads L2 instead of HBM
-      const int qn = q + (int)gridDim.x;
-      if (qn < P.b.num_q)
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
-                         P.q + (int64_t)qn * P.n_heads * kDim),
-                     "r"((uint32_t)(P.n_heads * kDim * 2))
-                     : "memory");
-    }
     // ---- row list and counts of this query (built one query ahead by the
-    // first softmax warp)
+    // O^T issuer's warp)
     const uint32_t ms_slot = qi & 1;
     if (!wait_bar(&ms->meta_full[ms_slot], (qi >> 1) & 1, ms)) break;
     const int *list = lists + ms_slot * kMaxSel;
@@ -456,42 +434,7 @@ __device__ void producer_role(const Params &P, const CUtensorMap *tmap_q, uint8_
     // in flight while a step waits for its buffer and is stored
     const int nsteps = nch * 2;
     Item b0[kItemsPerThread], b1[kItemsPerThread];
-    // the first step's rows are loaded before Q is converted: their latency
-    // overlaps the copy and the conversion
     load_step<kFp4>(list, S, row0, 0, b0);
-    if (!wait_bar(&ms->q_tma, qi & 1, ms)) break;
-    tma_pending = -1;
-    // in batches: every shared-memory read of a batch is issued before its
-    // conversions and stores
-    constexpr int kQBatch = 4;
-    const int q_chunks = P.n_heads * (kDim / 8);
-    for (int base = ptid; base < q_chunks; base += kQBatch * kProducerThreads) {
-      uint4 raw[kQBatch];
-      uint32_t off[kQBatch];
-#pragma unroll
-      for (int k = 0; k < kQBatch; ++k) {
-        const int it = base + k * kProducerThreads;
-        const int h = it / (kDim / 8), d = (it % (kDim / 8)) * 8;
-        off[k] = sw128_offset(h, d, kQBlock);
-        if (it < q_chunks) raw[k] = *reinterpret_cast<const uint4 *>(Qs + off[k]);
-      }
-#pragma unroll
-      for (int k = 0; k < kQBatch; ++k) {
-        if (base + k * kProducerThreads >= q_chunks) break;
-        const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
-        uint32_t o[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xffff0000u);
-          __half2 hh = __floats2half2_rn(lo, hi);
-          o[j] = *reinterpret_cast<uint32_t *>(&hh);
-        }
-        *reinterpret_cast<uint4 *>(Qs + off[k]) = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&ms->q_full);
     bool ok = true;
     // one step: prefetch step st+1 into `pre`, then store step st from `use`
     auto step = [&](int st, Item(&use)[kItemsPerThread], Item(&pre)[kItemsPerThread]) -> bool {
@@ -526,11 +469,6 @@ __device__ void producer_role(const Params &P, const CUtensorMap *tmap_q, uint8_
     }
     g += nch;
     if (!ok) break;
-  }
-  if (tma_pending >= 0) {   // an abort left a Q copy in flight: let it land
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(&ms->q_tma, (uint32_t)tma_pending) && globaltimer() - t0 < kWaitNs) {
-    }
   }
 }
 
@@ -603,30 +541,64 @@ __device__ void s_issuer_role(const Params &P, uint8_t *smem, Misc *ms) {
   __syncwarp();
 }
 
-// O^T issuer (lane 0 of warp kOWarp): O^T += R(g)^T . P(g)^T as soon as P(g) is
+// Row list and counts of query qn into slot qin & 1, by one whole warp
+// (query_rows), then meta_full[slot] is arrived on.  The O^T issuer's warp
+// builds them one query ahead of their use: at the start of its query qi it
+// publishes query qi + 1 into slot (qi + 1) & 1, which was last read for
+// query qi - 1 (by the producers while gathering its rows, all stored before
+// its last O^T could be issued, and by every role at that query's start).
+__device__ void publish_rows(const Params &P, uint8_t *smem, Misc *ms, int qn, uint32_t qin,
+                             int &err) {
+  if (qn >= P.b.num_q) return;
+  const int lane = threadIdx.x & 31;
+  int *lists = reinterpret_cast<int *>(smem + kOffList);
+  const uint32_t slot = qin & 1;
+  const Rows r1 = query_rows(P.b, qn, P.idx, P.k, P.win_lo, P.window, lists + slot * kMaxSel);
+  err |= r1.err;
+  const int64_t kv0 = P.b.kv_start[P.b.q_req[qn]];
+  __syncwarp();
+  if (lane == 0) {
+    ms->meta[slot][0] = r1.nsel;
+    ms->meta[slot][1] = r1.nwin;
+    ms->meta[slot][2] = r1.win_first;
+    ms->meta[slot][3] = kv0;
+    mbar_arrive(&ms->meta_full[slot]);
+  }
+}
+
+// O^T issuer (warp kOWarp, lane 0 issues): O^T += R(g)^T . P(g)^T as soon as P(g) is
 // written.  S^T(g) has completed by then (the softmax read it), so this
 // issuer's commits release R(g), half by half, for both products.
 __device__ void o_issuer_role(const Params &P, uint8_t *smem, Misc *ms) {
   const int lane = threadIdx.x & 31;
-  if (lane == 0) {
-    const uint32_t tmem = ms->tmem_base;
-    const uint32_t id_o = make_idesc_f16(128, kHeadsPad, true, true);
-    const Descs D = make_descs(smem);
-    bool ok = true;
-    uint32_t g = 0, qi = 0;
-    for (int q = blockIdx.x; q < P.b.num_q && ok; q += gridDim.x, ++qi) {
-      const uint32_t slot = qi & 1;
-      if (!(ok = wait_bar(&ms->meta_full[slot], (qi >> 1) & 1, ms))) break;
-      const int nch = n_chunks_of(ms->meta[slot][0] + ms->meta[slot][1]);
-      for (int c = 0; c < nch && ok; ++c, ++g) {
-        const uint32_t buf = g & 1, ph = (g >> 1) & 1;
-        ok = wait_bar(&ms->p_full[buf], ph, ms);
-        if (ok && c == 0) ok = wait_bar(&ms->o_empty, (qi & 1) ^ 1, ms);
-        if (!ok) break;
+  int err = 0;
+  publish_rows(P, smem, ms, blockIdx.x, 0, err);
+  const uint32_t tmem = ms->tmem_base;
+  const uint32_t id_o = make_idesc_f16(128, kHeadsPad, true, true);
+  const Descs D = make_descs(smem);
+  bool ok = true;
+  uint32_t g = 0, qi = 0;
+  // every lane waits (each acquires what it then reads); the outcome is made
+  // warp-uniform so that the whole warp leaves together on an abort
+  auto wait_all = [&](uint64_t *bar, uint32_t parity) {
+    const bool r = wait_bar(bar, parity, ms);
+    return __all_sync(0xffffffffu, r);
+  };
+  for (int q = blockIdx.x; q < P.b.num_q && ok; q += gridDim.x, ++qi) {
+    publish_rows(P, smem, ms, q + gridDim.x, qi + 1, err);
+    const uint32_t slot = qi & 1;
+    if (!(ok = wait_all(&ms->meta_full[slot], (qi >> 1) & 1))) break;
+    const int nch = n_chunks_of(ms->meta[slot][0] + ms->meta[slot][1]);
+    for (int c = 0; c < nch && ok; ++c, ++g) {
+      const uint32_t buf = g & 1, ph = (g >> 1) & 1;
+      ok = wait_all(&ms->p_full[buf], ph);
+      if (ok && c == 0) ok = wait_all(&ms->o_empty, (qi & 1) ^ 1);
+      if (!ok) break;
+      if (lane == 0) {
         fence_after_sync();
         const uint32_t ra = D.rm_lo + ((buf * kRBuf) >> 4), pa = D.p_lo + ((buf * kPBuf) >> 4);
-        // rows 0-31 of the chunk first, so the producers can refill that half
-        // while the second half is still being read
+        // rows 0-31 of the chunk first, so the producers can refill that
+        // half while the second half is still being read
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
 #pragma unroll
@@ -643,10 +615,13 @@ __device__ void o_issuer_role(const Params &P, uint8_t *smem, Misc *ms) {
         mma_commit(&ms->p_empty[buf]);
         if (c == nch - 1) mma_commit(&ms->o_full);
       }
+      __syncwarp();
     }
-    drain(&ms->done_o);
   }
+  if (lane == 0) drain(&ms->done_o);
   __syncwarp();
+  err = __reduce_or_sync(0xffffffffu, err);
+  if (lane == 0) raise_err(P.d_err, err);
 }
 
 // ---------------------------------------------------------------------------
@@ -663,35 +638,64 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
   float lsum[8];   // this thread's heads 32hh + 8k + hc + e, as [2k + e]
   uint32_t g = 0, qi = 0, gp = 0;
   bool ok = true;
-  int err = 0;
-  int *lists = reinterpret_cast<int *>(smem + kOffList);
-  // Row lists and counts are built by warp 0 one query ahead of their use.
-  // Slot (qi+1)&1 was last read for query qi-1, whose chunks have all been
-  // produced and consumed before this role reaches query qi.
-  auto publish = [&](int qn, uint32_t qin) {
-    if (warp != 0 || qn >= P.b.num_q) return;
-    const uint32_t slot = qin & 1;
-    const Rows r1 = query_rows(P.b, qn, P.idx, P.k, P.win_lo, P.window, lists + slot * kMaxSel);
-    err |= r1.err;
-    const int64_t kv0 = P.b.kv_start[P.b.q_req[qn]];
-    __syncwarp();
-    if (lane == 0) {
-      ms->meta[slot][0] = r1.nsel;
-      ms->meta[slot][1] = r1.nwin;
-      ms->meta[slot][2] = r1.win_first;
-      ms->meta[slot][3] = kv0;
-      mbar_arrive(&ms->meta_full[slot]);
+  // Q of query qn into the f16 operand buffer: bf16 rows read 16 bytes at a
+  // time (from L2: the copy was prefetched a query ahead), converted, and
+  // stored at their SW128 positions; heads past n_heads stay zero (written
+  // once below).  Then the S^T issuer may start the query.
+  uint8_t *Qs = smem + kOffQ;
+  auto load_q = [&](int qn) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(P.q + (int64_t)qn * P.n_heads * kDim);
+    const int q_chunks = P.n_heads * (kDim / 8);
+    constexpr int kQBatch = 8;
+    for (int base = stid; base < q_chunks; base += kQBatch * kSoftmaxWarps * 32) {
+      uint4 raw[kQBatch];
+#pragma unroll
+      for (int k = 0; k < kQBatch; ++k) {
+        const int it = base + k * kSoftmaxWarps * 32;
+        if (it < q_chunks) raw[k] = __ldg(src + it);
+      }
+#pragma unroll
+      for (int k = 0; k < kQBatch; ++k) {
+        const int it = base + k * kSoftmaxWarps * 32;
+        if (it >= q_chunks) break;
+        const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xffff0000u);
+          __half2 h2 = __floats2half2_rn(lo, hi);
+          o[j] = *reinterpret_cast<uint32_t *>(&h2);
+        }
+        const int h = it / (kDim / 8), d = (it % (kDim / 8)) * 8;
+        *reinterpret_cast<uint4 *>(Qs + sw128_offset(h, d, kQBlock)) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+      }
     }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ms->q_full);
   };
-  publish(blockIdx.x, 0);
+  auto prefetch_q = [&](int qn) {
+    if (stid == 0 && qn < P.b.num_q)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                       P.q + (int64_t)qn * P.n_heads * kDim),
+                   "r"((uint32_t)(P.n_heads * kDim * 2))
+                   : "memory");
+  };
   if (stid < 64) ms->m_ref[stid] = NEG_INF;
+  for (int it = P.n_heads * (kDim / 8) + stid; it < kHeadsPad * (kDim / 8);
+       it += kSoftmaxWarps * 32) {
+    const int h = it / (kDim / 8), d = (it % (kDim / 8)) * 8;
+    *reinterpret_cast<uint4 *>(Qs + sw128_offset(h, d, kQBlock)) = make_uint4(0, 0, 0, 0);
+  }
+  if (blockIdx.x < P.b.num_q) load_q(blockIdx.x);
   ok = group_sync(&ms->sm_grp, gp, ms);
   for (int q = blockIdx.x; q < P.b.num_q && ok; q += gridDim.x, ++qi) {
     const uint32_t slot = qi & 1;
     if (!(ok = wait_bar(&ms->meta_full[slot], (qi >> 1) & 1, ms))) break;
     const int64_t nrows = ms->meta[slot][0] + ms->meta[slot][1];
     const int nch = n_chunks_of(nrows);
-    publish(q + gridDim.x, qi + 1);
+    prefetch_q(q + gridDim.x);
 #pragma unroll
     for (int j = 0; j < 8; ++j) lsum[j] = 0.f;
     for (int c = 0; c < nch; ++c, ++g) {
@@ -820,6 +824,13 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
       if (lane == 0) mbar_arrive(&ms->p_full[sb]);
     }
     if (!ok) break;
+    // ---- the next query's Q, as soon as this query's last S^T has read the
+    // buffer (before this query's epilogue, so that the next query's first
+    // products overlap it)
+    if (q + (int)gridDim.x < P.b.num_q) {
+      if (!(ok = wait_bar(&ms->q_empty, qi & 1, ms))) break;
+      load_q(q + gridDim.x);
+    }
     // ---- epilogue: row sums, normalisation, bf16 output, lse
     // per head: over the 8 threads holding its columns, then across the warps
     {
@@ -874,22 +885,17 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
     __syncwarp();
     if (lane == 0) mbar_arrive(&ms->o_empty);
   }
-  if (warp == 0) {
-    err = __reduce_or_sync(0xffffffffu, err);
-    if (lane == 0) raise_err(P.d_err, err);
-  }
 }
 
 template <bool kFp4>
 __global__ void __launch_bounds__(kThreads, 1)
-attn_tc_kernel(Params P, const __grid_constant__ CUtensorMap tmap_q) {
+attn_tc_kernel(Params P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Misc *ms = reinterpret_cast<Misc *>(smem + kOffMisc);
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    mbar_init(&ms->q_full, kProducerWarps);
+    mbar_init(&ms->q_full, kSoftmaxWarps);
     mbar_init(&ms->q_empty, 1);
-    mbar_init(&ms->q_tma, 1);
     mbar_init(&ms->o_full, 1);
     mbar_init(&ms->o_empty, kSoftmaxWarps);
     mbar_init(&ms->done, 1);
@@ -923,7 +929,7 @@ attn_tc_kernel(Params P, const __grid_constant__ CUtensorMap tmap_q) {
   } else if (warp == kOWarp) {
     o_issuer_role(P, smem, ms);
   } else {
-    producer_role<kFp4>(P, &tmap_q, smem, ms);
+    producer_role<kFp4>(P, smem, ms);
   }
   fence_before_sync();
   __syncthreads();
@@ -932,22 +938,6 @@ attn_tc_kernel(Params P, const __grid_constant__ CUtensorMap tmap_q) {
     fence_after_sync();
     tmem_dealloc(ms->tmem_base, kTmemCols);
   }
-}
-
-// Q [num_q, n_heads, 512] bf16 as a 3-D map (dims, heads, queries) with
-// 64 x 64 x 1 boxes in 128-byte swizzle: one box is one 64-channel block of
-// the SW128 operand tile; heads past n_heads read as zeros.
-bool make_q_map(CUtensorMap *map, const __nv_bfloat16 *q, int n_heads, int num_q) {
-  EncodeTiled fn = encode_tiled();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)kDim, (cuuint64_t)n_heads, (cuuint64_t)num_q};
-  const cuuint64_t strides[2] = {(cuuint64_t)kDim * 2, (cuuint64_t)n_heads * kDim * 2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)kHeadsPad, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16 *>(q), dims,
-            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -984,16 +974,14 @@ int attn_tc(const Batch &b, int n_heads, const __nv_bfloat16 *q, const uint8_t *
   P.d_err = d_err;
   P.wait_ns = wait_limit_ns();
   const int grid = b.num_q < sm_count() ? b.num_q : sm_count();
-  CUtensorMap tmap_q;
-  if (!make_q_map(&tmap_q, q, n_heads, b.num_q)) return CSA2_ERR_UNSUPPORTED;
   if (kv_sf) {
     cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)kSmemBytes);
-    attn_tc_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(P, tmap_q);
+    attn_tc_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(P);
   } else {
     cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)kSmemBytes);
-    attn_tc_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(P, tmap_q);
+    attn_tc_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(P);
   }
   return launch_status();
 }
