@@ -720,7 +720,8 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
       float x[16], mr[8];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float2 m2 = *reinterpret_cast<const float2 *>(&ms->m_ref[32 * hh + 8 * k + hc]);
+        const float2 m2 = c == 0 ? make_float2(NEG_INF, NEG_INF)
+                                 : *reinterpret_cast<const float2 *>(&ms->m_ref[32 * hh + 8 * k + hc]);
         mr[2 * k] = m2.x;
         mr[2 * k + 1] = m2.y;
       }
@@ -736,7 +737,9 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
       const bool vote = __any_sync(0xffffffffu, exceed);
       if (lane == 0) ms->votes[vb][warp] = vote ? 1 : 0;
       if (!(ok = group_sync(&ms->sm_grp, gp, ms))) break;
-      bool slow = false;
+      // the first chunk of a query always sets the reference (from an empty
+      // one: -inf when no row of the chunk is valid)
+      bool slow = c == 0;
 #pragma unroll
       for (int w = 0; w < kSoftmaxWarps; ++w) slow |= ms->votes[vb][w] != 0;
       if (slow) {
@@ -763,7 +766,7 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
         }
         if (!(ok = group_sync(&ms->sm_grp, gp, ms))) break;
         if (stid < 64) {
-          const float old = ms->m_ref[stid];
+          const float old = c == 0 ? NEG_INF : ms->m_ref[stid];
           float mx = fmaxf(fmaxf(ms->red[0][stid], ms->red[1][stid]),
                            fmaxf(ms->red[2][stid], ms->red[3][stid]));
           mx = fmaxf(mx, old);
@@ -849,18 +852,22 @@ __device__ void softmax_role(const Params &P, uint8_t *smem, Misc *ms) {
       }
     }
     if (!(ok = group_sync(&ms->sm_grp, gp, ms))) break;
-    if (stid < 64) {
-      float l = (ms->red[0][stid] + ms->red[1][stid]) + (ms->red[2][stid] + ms->red[3][stid]);
-      const float m = ms->m_ref[stid];
+    {
+      // every warp derives the normalisers of its own head half (lane j:
+      // head 32hh + j; the four warps of a half write the same values), so
+      // no second barrier is needed before the output; the next query's
+      // first chunk starts from an empty reference instead of a reset one
+      const int h = 32 * hh + lane;
+      float l = (ms->red[0][h] + ms->red[1][h]) + (ms->red[2][h] + ms->red[3][h]);
+      const float m = ms->m_ref[h];
       const float mu = m == NEG_INF ? 0.f : m;
-      if (P.sink && stid < P.n_heads) l += exp2f(P.sink[stid] * 1.4426950408889634f - mu);
-      ms->alpha[stid] = l > 0.f ? 1.f / l : 0.f;
-      if (P.lse && stid < P.n_heads)
-        P.lse[(int64_t)q * P.n_heads + stid] =
+      if (P.sink && h < P.n_heads) l += exp2f(P.sink[h] * 1.4426950408889634f - mu);
+      ms->alpha[h] = l > 0.f ? 1.f / l : 0.f;
+      if (sp == 0 && P.lse && h < P.n_heads)
+        P.lse[(int64_t)q * P.n_heads + h] =
             l > 0.f ? (mu + log2f(l)) * 0.6931471805599453f : NEG_INF;
-      ms->m_ref[stid] = NEG_INF;   // reference of the next query
+      __syncwarp();
     }
-    if (!(ok = group_sync(&ms->sm_grp, gp, ms))) break;
     ok = wait_bar(&ms->o_full, qi & 1, ms);
     if (!ok) break;
     fence_after_sync();
