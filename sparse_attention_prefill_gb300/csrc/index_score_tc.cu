@@ -20,12 +20,13 @@
 // held to 1e-5 of sum_h |w_h| ReLU(dot_h).
 //
 // Work unit (one CTA): a tile of 256/Hi consecutive query rows and a chunk of
-// 32 key tiles (4096 keys or pool slots).  Rows of the tile that belong to the
-// same request share key tiles ("runs", full mode); in pool mode every query
-// has its own slot list and is its own run, except that identity pools
-// (blocks 0, 1, ..., nb-1: nothing excluded, the case when every reachable
-// position fits the pool budget) map slot s to entry s and merge like full
-// mode.  Roles (16 warps):
+// key tiles: 128 (16384 keys) over full rows no longer than that, else 64;
+// 32 (4096 slots) in pool mode.
+// Rows of the tile that belong to the same request share key tiles ("runs",
+// full mode); in pool mode every query has its own slot list and is its own
+// run, except that identity pools (blocks 0, 1, ..., nb-1: nothing excluded,
+// the case when every reachable position fits the pool budget) map slot s to
+// entry s and merge like full mode.  Roles (16 warps):
 //   warps 0-7   epilogue (warp w: TMEM lanes 32*(w%4).., queries of parity w/4)
 //   warp 8      TMEM allocation; lane 0 issues the MMAs
 //   warps 9-15  producers: key gather + E2M1 -> f16 into a 4-stage ring, one
@@ -46,7 +47,12 @@ namespace {
 using namespace tc;
 
 constexpr int kKeyTile = 128;
-constexpr int kTilesPerChunk = 32;
+// key tiles per CTA: over full rows 128 (16384 keys) when one chunk covers
+// the longest row, so that each query tile is one CTA, else 64; in pool mode
+// 32 (4096 slots), whose candidate blocks are copied to shared memory
+constexpr int kTilesWhole = 128;
+constexpr int kTilesFull = 64;
+constexpr int kTilesPool = 32;
 constexpr int kStages = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kMmaWarp = 8;
@@ -157,6 +163,7 @@ struct Params {
   int block, max_blocks;
   float *scores;
   int64_t ld;          // row capacity in entries (rows past it are cut, CSA2_DERR_LD)
+  int tpc;             // key tiles per CTA chunk
   int64_t out_ld;      // row stride of `scores` (sample mode: ld / stride tiles)
   int stride;          // 1: every key tile; S: tiles 0, S, 2S, .. only, stored densely
   // list mode (list_cnt != nullptr): no dense scores; each query appends the
@@ -252,27 +259,27 @@ __device__ __forceinline__ void load_tile(const Params &P, const Misc *ms, const
 
 // next (run, tile) after (ri, kt) within key chunk y; false when none is left
 template <int STRIDE>
-__device__ __forceinline__ bool next_item(const Misc *ms, int y, int &ri, int64_t &kt) {
+__device__ __forceinline__ bool next_item(const Misc *ms, int y, int tpc, int &ri, int64_t &kt) {
   ++kt;
   while (ri < ms->nruns) {
     const int64_t nt = walked_tiles<STRIDE>(ms->runs[ri].len);
-    const int64_t hi = min(nt, (int64_t)(y + 1) * kTilesPerChunk);
+    const int64_t hi = min(nt, (int64_t)(y + 1) * tpc);
     if (kt < hi) return true;
     ++ri;
-    kt = (int64_t)y * kTilesPerChunk;
+    kt = (int64_t)y * tpc;
   }
   return false;
 }
 
-template <int STRIDE>
+template <int STRIDE, int TPC>
 __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms, int q0, int y) {
   const int ptid = threadIdx.x - kProdWarp0 * 32;
   const int lane = threadIdx.x & 31;
   int err = 0;
   uint32_t it = 0;
   int ri = 0;
-  int64_t kt = (int64_t)y * kTilesPerChunk - 1;
-  if (!next_item<STRIDE>(ms, y, ri, kt)) return;
+  int64_t kt = (int64_t)y * TPC - 1;
+  if (!next_item<STRIDE>(ms, y, TPC, ri, kt)) return;
   KeyLoad ka, kb;
   const CandView cv = cand_view(P, ms, smem);
   load_tile<STRIDE>(P, ms, cv, ri, kt, q0, ptid, ka);
@@ -282,7 +289,7 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
   auto step = [&](KeyLoad &use, KeyLoad &pre) -> bool {
     int ri2 = ri;
     int64_t kt2 = kt;
-    more = next_item<STRIDE>(ms, y, ri2, kt2);
+    more = next_item<STRIDE>(ms, y, TPC, ri2, kt2);
     if (more) load_tile<STRIDE>(P, ms, cv, ri2, kt2, q0, ptid, pre);
     const uint32_t st = it % kStages;
     if (!wait_bar(&ms->a_empty[st], ((it / kStages) & 1) ^ 1, ms)) return false;
@@ -325,7 +332,7 @@ __device__ void producer_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
   if (lane == 0) raise_err(P.d_err, err);
 }
 
-template <int STRIDE>
+template <int STRIDE, int TPC>
 __device__ void mma_role(const Params &P, uint8_t *smem, Misc *ms, int y) {
   const int lane = threadIdx.x & 31;
   if (lane == 0) {
@@ -340,8 +347,8 @@ __device__ void mma_role(const Params &P, uint8_t *smem, Misc *ms, int y) {
       n = (n + 15u) & ~15u;
       const uint32_t idesc = make_idesc_f16(128, n, false, false);
       const uint32_t brow = (uint32_t)(ru.ql0 * P.hi) * 128u;   // byte offset of the run's rows
-      for (int64_t kt = (int64_t)y * kTilesPerChunk;
-           kt < nt && kt < (int64_t)(y + 1) * kTilesPerChunk; ++kt, ++it) {
+      for (int64_t kt = (int64_t)y * TPC;
+           kt < nt && kt < (int64_t)(y + 1) * TPC; ++kt, ++it) {
         const uint32_t st = it % kStages, db = it & 1;
         if (!(ok = wait_bar(&ms->a_full[st], (it / kStages) & 1, ms))) break;
         if (!(ok = wait_bar(&ms->d_empty[db], ((it >> 1) & 1) ^ 1, ms))) break;
@@ -366,7 +373,7 @@ __device__ void mma_role(const Params &P, uint8_t *smem, Misc *ms, int y) {
   __syncwarp();
 }
 
-template <int HI, bool kList, int STRIDE>
+template <int HI, bool kList, int STRIDE, int TPC>
 __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, int y) {
   const CandView cv = cand_view(P, ms, smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -380,8 +387,8 @@ __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
   for (int ri = 0; ri < ms->nruns && ok; ++ri) {
     const RunInfo ru = ms->runs[ri];
     const int64_t nt = walked_tiles<STRIDE>(ru.len);
-    for (int64_t kt = (int64_t)y * kTilesPerChunk;
-         kt < nt && kt < (int64_t)(y + 1) * kTilesPerChunk; ++kt, ++it) {
+    for (int64_t kt = (int64_t)y * TPC;
+         kt < nt && kt < (int64_t)(y + 1) * TPC; ++kt, ++it) {
       const uint32_t db = it & 1;
       if (!(ok = wait_bar(&ms->d_full[db], (it >> 1) & 1, ms))) break;
       fence_after_sync();
@@ -479,7 +486,7 @@ __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
 
 // MODE 0: dense score rows; 1: sample (every kStreamStride-th key tile,
 // stored densely); 2: appending lists
-template <int HI, int MODE>
+template <int HI, int MODE, int TPC>
 __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
   constexpr int STRIDE = MODE == 1 ? kStreamStride : 1;
   constexpr bool kList = MODE == 2;
@@ -520,8 +527,8 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
   // the end), and the slots of the chunk map through an identity pool iff the
   // last present block of the range is its own index (blocks are strictly
   // ascending, so block i >= i, with equality all the way down)
-  const int64_t s_lo = (int64_t)y * kKeyTile * kTilesPerChunk;
-  const int64_t s_hi = s_lo + (int64_t)kKeyTile * kTilesPerChunk;
+  const int64_t s_lo = (int64_t)y * kKeyTile * TPC;
+  const int64_t s_hi = s_lo + (int64_t)kKeyTile * TPC;
   int b_lo = 0, b_hi = 0;
   if (P.cand) {
     b_lo = (int)(s_lo / P.block);
@@ -635,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
   // does this CTA's key chunk hold any work?
   bool any = false;
   for (int ri = 0; ri < ms->nruns; ++ri)
-    any |= walked_tiles<STRIDE>(ms->runs[ri].len) > (int64_t)y * kTilesPerChunk;
+    any |= walked_tiles<STRIDE>(ms->runs[ri].len) > (int64_t)y * TPC;
   if (!any) {
     raise_err(P.d_err, err);
     return;
@@ -676,11 +683,11 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
     fence_after_sync();
   }
   if (warp < kEpiWarps) {
-    epilogue_role<HI, kList, STRIDE>(P, smem, ms, q0, y);
+    epilogue_role<HI, kList, STRIDE, TPC>(P, smem, ms, q0, y);
   } else if (warp == kMmaWarp) {
-    mma_role<STRIDE>(P, smem, ms, y);
+    mma_role<STRIDE, TPC>(P, smem, ms, y);
   } else {
-    producer_role<STRIDE>(P, smem, ms, q0, y);
+    producer_role<STRIDE, TPC>(P, smem, ms, q0, y);
   }
   err = __reduce_or_sync(0xffffffffu, err);
   if ((threadIdx.x & 31) == 0) raise_err(P.d_err, err);
@@ -702,26 +709,27 @@ int launch(Params &P, int n_heads, cudaStream_t st) {
   int64_t max_len = P.cand ? (int64_t)P.max_blocks * P.block : P.ld;
   if (max_len > P.ld) max_len = P.ld;
   const int64_t tiles_walked = (((max_len + kKeyTile - 1) / kKeyTile) + P.stride - 1) / P.stride;
-  const int64_t chunks = (tiles_walked + kTilesPerChunk - 1) / kTilesPerChunk;
+  P.tpc = P.cand ? kTilesPool
+                 : (P.stride == 1 && !P.list_cnt && tiles_walked <= kTilesWhole) ? kTilesWhole
+                                                                                  : kTilesFull;
+  const int64_t chunks = (tiles_walked + P.tpc - 1) / P.tpc;
   if (chunks == 0) return CSA2_OK;
   if (chunks > 65535) return CSA2_ERR_UNSUPPORTED;
   const int64_t tiles = (P.b.num_q + P.qt - 1) / P.qt;
   dim3 grid((unsigned)tiles, (unsigned)chunks);
+#define CSA2_GO(H, M, T)                                                                     \
+  do {                                                                                       \
+    cudaFuncSetAttribute(index_score_tc_kernel<H, M, T>,                                     \
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);      \
+    index_score_tc_kernel<H, M, T><<<grid, kThreads, kSmemBytes, st>>>(P);                   \
+  } while (0)
 #define CSA2_LAUNCH(H)                                                                       \
   do {                                                                                       \
-    if (P.list_cnt) {                                                                        \
-      cudaFuncSetAttribute(index_score_tc_kernel<H, 2>,                                      \
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);    \
-      index_score_tc_kernel<H, 2><<<grid, kThreads, kSmemBytes, st>>>(P);                    \
-    } else if (P.stride != 1) {                                                              \
-      cudaFuncSetAttribute(index_score_tc_kernel<H, 1>,                                      \
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);    \
-      index_score_tc_kernel<H, 1><<<grid, kThreads, kSmemBytes, st>>>(P);                    \
-    } else {                                                                                 \
-      cudaFuncSetAttribute(index_score_tc_kernel<H, 0>,                                      \
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);    \
-      index_score_tc_kernel<H, 0><<<grid, kThreads, kSmemBytes, st>>>(P);                    \
-    }                                                                                        \
+    if (P.list_cnt) CSA2_GO(H, 2, kTilesFull);                                               \
+    else if (P.stride != 1) CSA2_GO(H, 1, kTilesFull);                                       \
+    else if (P.cand) CSA2_GO(H, 0, kTilesPool);                                              \
+    else if (P.tpc == kTilesWhole) CSA2_GO(H, 0, kTilesWhole);                               \
+    else CSA2_GO(H, 0, kTilesFull);                                                          \
   } while (0)
   switch (n_heads) {
     case 8: CSA2_LAUNCH(8); break;
@@ -731,6 +739,7 @@ int launch(Params &P, int n_heads, cudaStream_t st) {
     default: return CSA2_ERR_UNSUPPORTED;
   }
 #undef CSA2_LAUNCH
+#undef CSA2_GO
   return launch_status();
 }
 
