@@ -493,7 +493,10 @@ __global__ void __launch_bounds__(kThreads, 1) index_score_tc_kernel(Params P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Misc *ms = reinterpret_cast<Misc *>(smem + kOffMisc);
   constexpr int QT = 256 / HI;
-  const int q0 = blockIdx.x * QT;
+  // query tiles are taken in reverse order: in a causal batch the later
+  // tiles have the longer rows, and starting those first keeps the last wave
+  // of CTAs short
+  const int q0 = (int)(gridDim.x - 1 - blockIdx.x) * QT;
   const int y = blockIdx.y;
   const int warp = threadIdx.x >> 5;
   int err = 0;
