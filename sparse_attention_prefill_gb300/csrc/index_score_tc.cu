@@ -20,8 +20,8 @@
 // held to 1e-5 of sum_h |w_h| ReLU(dot_h).
 //
 // Work unit (one CTA): a tile of 256/Hi consecutive query rows and a chunk of
-// key tiles: 128 (16384 keys) over full rows no longer than that, else 64;
-// 32 (4096 slots) in pool mode.
+// key tiles: 128 (16384 keys, or 128 sampled tiles) when that covers the
+// longest row, else 64; 32 (4096 slots) in pool mode.
 // Rows of the tile that belong to the same request share key tiles ("runs",
 // full mode); in pool mode every query has its own slot list and is its own
 // run, except that identity pools (blocks 0, 1, ..., nb-1: nothing excluded,
@@ -712,9 +712,7 @@ int launch(Params &P, int n_heads, cudaStream_t st) {
   int64_t max_len = P.cand ? (int64_t)P.max_blocks * P.block : P.ld;
   if (max_len > P.ld) max_len = P.ld;
   const int64_t tiles_walked = (((max_len + kKeyTile - 1) / kKeyTile) + P.stride - 1) / P.stride;
-  P.tpc = P.cand ? kTilesPool
-                 : (P.stride == 1 && !P.list_cnt && tiles_walked <= kTilesWhole) ? kTilesWhole
-                                                                                  : kTilesFull;
+  P.tpc = P.cand ? kTilesPool : tiles_walked <= kTilesWhole ? kTilesWhole : kTilesFull;
   const int64_t chunks = (tiles_walked + P.tpc - 1) / P.tpc;
   if (chunks == 0) return CSA2_OK;
   if (chunks > 65535) return CSA2_ERR_UNSUPPORTED;
@@ -728,7 +726,9 @@ int launch(Params &P, int n_heads, cudaStream_t st) {
   } while (0)
 #define CSA2_LAUNCH(H)                                                                       \
   do {                                                                                       \
-    if (P.list_cnt) CSA2_GO(H, 2, kTilesFull);                                               \
+    if (P.list_cnt && P.tpc == kTilesWhole) CSA2_GO(H, 2, kTilesWhole);                      \
+    else if (P.list_cnt) CSA2_GO(H, 2, kTilesFull);                                          \
+    else if (P.stride != 1 && P.tpc == kTilesWhole) CSA2_GO(H, 1, kTilesWhole);              \
     else if (P.stride != 1) CSA2_GO(H, 1, kTilesFull);                                       \
     else if (P.cand) CSA2_GO(H, 0, kTilesPool);                                              \
     else if (P.tpc == kTilesWhole) CSA2_GO(H, 0, kTilesWhole);                               \
