@@ -18,8 +18,8 @@ L20-style source, L21-style Reindex in the pool, L22-style Reuse over 1024
 tail rows) is measured too and reported under "c2_decoder_replay", with the
 FP4 main-KV attention, the tail cut / scatter-back and the cache writes.
 
---impl reference times the CPU oracle (the baseline arm of this build) on a
-bounded sample of the same workload.
+--impl reference times the CPU oracle (the reference arm: a plain restatement
+of the method in double precision) on a bounded sample of the same workload.
 """
 import argparse
 import json
