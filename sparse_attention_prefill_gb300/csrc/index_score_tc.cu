@@ -422,6 +422,34 @@ __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
           P.list_val[o] = outv;
         }
       };
+      // list mode in two halves: reserve() takes the warp's slots for a query
+      // with one atomic whose result is only read by commit(), so that the
+      // atomics of one round are in flight while the next round's columns
+      // are loaded and reduced
+      struct Rsv {
+        uint32_t m, base;
+        int ql;
+        float outv;
+      };
+      auto reserve = [&](int ql, float acc, Rsv &r) {
+        const bool in = s < ms->row_len[ql];
+        r.ql = ql;
+        r.outv = acc;
+        r.base = 0u;
+        r.m = __ballot_sync(0xffffffffu, in && acc >= ms->thr[ql]);
+        if (r.m != 0u && lane == __ffs(r.m) - 1)
+          r.base = atomicAdd(P.list_cnt + q0 + ql, (uint32_t)__popc(r.m));
+      };
+      auto commit = [&](const Rsv &r) {
+        if (r.m == 0u) return;
+        const uint32_t base = __shfl_sync(0xffffffffu, r.base, __ffs(r.m) - 1) +
+                              __popc(r.m & ((1u << lane) - 1u));
+        if (((r.m >> lane) & 1u) && base < (uint32_t)P.list_cap) {
+          const int64_t o = (int64_t)(q0 + r.ql) * P.list_cap + base;
+          P.list_ent[o] = s;
+          P.list_val[o] = r.outv;
+        }
+      };
       // w * ReLU(x) as (w/2) * (x + |x|): the same value (halving and
       // doubling are exact), on the FMA pipe instead of a min/max on the ALU
       // pipe.  ms->w holds w/2.
@@ -444,7 +472,30 @@ __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
         }
         return (a01.x + a01.y) + (a23.x + a23.y);
       };
-      if constexpr (HI == 32) {
+      if constexpr (HI == 32 && kList) {
+        // as below, with the list appends of each round committed after the
+        // next round's reductions (full mode: no candidate blocks)
+        Rsv p0, p1;
+        bool pend0 = false, pend1 = false;
+        for (int qq = par; qq < ru.nq; qq += 4) {
+          const bool two = qq + 2 < ru.nq;   // uniform across the warp
+          uint32_t v0[32], v1[32];
+          const uint32_t col = db * 256 + (uint32_t)(qq * HI);
+          tmem_ld32x32b_x32(tmem + lane_addr + col, v0);
+          if (two) tmem_ld32x32b_x32(tmem + lane_addr + col + 2 * HI, v1);
+          tmem_wait_ld();
+          const float a0 = dot(ru.ql0 + qq, 0, v0, 32, 0.f);
+          const float a1 = two ? dot(ru.ql0 + qq + 2, 0, v1, 32, 0.f) : 0.f;
+          if (pend0) commit(p0);
+          if (pend1) commit(p1);
+          reserve(ru.ql0 + qq, a0, p0);
+          pend0 = true;
+          pend1 = two;
+          if (two) reserve(ru.ql0 + qq + 2, a1, p1);
+        }
+        if (pend0) commit(p0);
+        if (pend1) commit(p1);
+      } else if constexpr (HI == 32) {
         // two queries' columns in flight per TMEM wait
         for (int qq = par; qq < ru.nq; qq += 4) {
           const bool two = qq + 2 < ru.nq;   // uniform across the warp
