@@ -384,6 +384,36 @@ __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
   constexpr int NL = HI / LW;                // loads per query
   uint32_t it = 0;
   bool ok = true;
+  // list mode in two halves: reserve() takes the warp's slots for a query
+  // with one atomic whose result is only read by commit(), one round of
+  // reductions later (the pending pair is carried across key tiles)
+  struct Rsv {
+    uint32_t m, base;
+    int ql, s;
+    float outv;
+  };
+  auto reserve = [&](int ql, int s, float acc, Rsv &r) {
+    const bool in = s < ms->row_len[ql];
+    r.ql = ql;
+    r.s = s;
+    r.outv = acc;
+    r.base = 0u;
+    r.m = __ballot_sync(0xffffffffu, in && acc >= ms->thr[ql]);
+    if (r.m != 0u && lane == __ffs(r.m) - 1)
+      r.base = atomicAdd(P.list_cnt + q0 + ql, (uint32_t)__popc(r.m));
+  };
+  auto commit = [&](const Rsv &r) {
+    if (r.m == 0u) return;
+    const uint32_t base = __shfl_sync(0xffffffffu, r.base, __ffs(r.m) - 1) +
+                          __popc(r.m & ((1u << lane) - 1u));
+    if (((r.m >> lane) & 1u) && base < (uint32_t)P.list_cap) {
+      const int64_t o = (int64_t)(q0 + r.ql) * P.list_cap + base;
+      P.list_ent[o] = r.s;
+      P.list_val[o] = r.outv;
+    }
+  };
+  Rsv p0, p1;
+  bool pend0 = false, pend1 = false;
   for (int ri = 0; ri < ms->nruns && ok; ++ri) {
     const RunInfo ru = ms->runs[ri];
     const int64_t nt = walked_tiles<STRIDE>(ru.len);
@@ -422,34 +452,6 @@ __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
           P.list_val[o] = outv;
         }
       };
-      // list mode in two halves: reserve() takes the warp's slots for a query
-      // with one atomic whose result is only read by commit(), so that the
-      // atomics of one round are in flight while the next round's columns
-      // are loaded and reduced
-      struct Rsv {
-        uint32_t m, base;
-        int ql;
-        float outv;
-      };
-      auto reserve = [&](int ql, float acc, Rsv &r) {
-        const bool in = s < ms->row_len[ql];
-        r.ql = ql;
-        r.outv = acc;
-        r.base = 0u;
-        r.m = __ballot_sync(0xffffffffu, in && acc >= ms->thr[ql]);
-        if (r.m != 0u && lane == __ffs(r.m) - 1)
-          r.base = atomicAdd(P.list_cnt + q0 + ql, (uint32_t)__popc(r.m));
-      };
-      auto commit = [&](const Rsv &r) {
-        if (r.m == 0u) return;
-        const uint32_t base = __shfl_sync(0xffffffffu, r.base, __ffs(r.m) - 1) +
-                              __popc(r.m & ((1u << lane) - 1u));
-        if (((r.m >> lane) & 1u) && base < (uint32_t)P.list_cap) {
-          const int64_t o = (int64_t)(q0 + r.ql) * P.list_cap + base;
-          P.list_ent[o] = s;
-          P.list_val[o] = r.outv;
-        }
-      };
       // w * ReLU(x) as (w/2) * (x + |x|): the same value (halving and
       // doubling are exact), on the FMA pipe instead of a min/max on the ALU
       // pipe.  ms->w holds w/2.
@@ -475,8 +477,6 @@ __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
       if constexpr (HI == 32 && kList) {
         // as below, with the list appends of each round committed after the
         // next round's reductions (full mode: no candidate blocks)
-        Rsv p0, p1;
-        bool pend0 = false, pend1 = false;
         for (int qq = par; qq < ru.nq; qq += 4) {
           const bool two = qq + 2 < ru.nq;   // uniform across the warp
           uint32_t v0[32], v1[32];
@@ -488,13 +488,11 @@ __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
           const float a1 = two ? dot(ru.ql0 + qq + 2, 0, v1, 32, 0.f) : 0.f;
           if (pend0) commit(p0);
           if (pend1) commit(p1);
-          reserve(ru.ql0 + qq, a0, p0);
+          reserve(ru.ql0 + qq, s, a0, p0);
           pend0 = true;
           pend1 = two;
-          if (two) reserve(ru.ql0 + qq + 2, a1, p1);
+          if (two) reserve(ru.ql0 + qq + 2, s, a1, p1);
         }
-        if (pend0) commit(p0);
-        if (pend1) commit(p1);
       } else if constexpr (HI == 32) {
         // two queries' columns in flight per TMEM wait
         for (int qq = par; qq < ru.nq; qq += 4) {
@@ -533,6 +531,8 @@ __device__ void epilogue_role(const Params &P, uint8_t *smem, Misc *ms, int q0, 
       if (lane == 0) mbar_arrive(&ms->d_empty[db]);
     }
   }
+  if (pend0) commit(p0);
+  if (pend1) commit(p1);
 }
 
 // MODE 0: dense score rows; 1: sample (every kStreamStride-th key tile,
