@@ -103,6 +103,29 @@ def test_index_score_full_mode(ratio, hi):
     assert int(d_err.item()) == rerr
 
 
+@pytest.mark.parametrize("ctx", [16384, 16385])
+def test_index_score_chunk_sizes(ctx):
+    """Rows at the key-tile chunk boundaries: a CTA covers 128 key tiles when
+    the longest row fits them (16384 entries) and 64 otherwise (16385); rows of
+    8192/8193 and 16384/16385 entries end at or just past a chunk."""
+    qpos = [8191, 8192, 8193, 16383, ctx - 1, 100]
+    w = synth.full_layer(ctx, 1, qpos, 16, 32, seed=13, tag="ichunk%d" % ctx)
+    b = w.batch("full")
+    L = w.layers["full"]
+    ref, rerr = O.index_score(np_batch(b), npy(L.q_fp4), npy(L.q_scale), npy(L.head_w),
+                              npy(w.pool.k_fp4), npy(w.pool.k_scale), w.ld)
+    d_err = _derr()
+    got = torch.full((w.num_q, w.ld), float("nan"), device=DEV)
+    S.index_score(_to(b), L.q_fp4.to(DEV), L.q_scale.to(DEV), L.head_w.to(DEV),
+                  w.pool.k_fp4.to(DEV), w.pool.k_scale.to(DEV), w.ld, scores=got, d_err=d_err)
+    g = npy(got)
+    tol = _score_tol(np_batch(b), w, "full", ref)
+    written = ~np.isnan(ref)
+    assert (np.isnan(g) == ~written).all()
+    assert (np.abs(g[written] - ref[written]) <= tol[written]).all()
+    assert int(d_err.item()) == rerr
+
+
 @pytest.mark.parametrize("hi", [32, 16, 8])
 def test_index_score_pool_mode_and_ctx_flag(hi):
     # hi = 32 keeps a CTA's candidate blocks in shared memory; 16 and 8 (more
