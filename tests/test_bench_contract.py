@@ -107,3 +107,23 @@ def test_roofline_counts_match_brute_force():
         assert bench.attn_launch_bytes(b, None, None, window, heads) == (
             int(bench.window_rows(b, None, window).sum()) * 576 + nq * (heads * 512 * 4 + heads * 4))
     assert bench.index_score_flops(10, 32) == 2 * 10 * 32 * 128
+
+
+def test_traffic_record_only_for_the_measured_kernel(tmp_path, monkeypatch):
+    """The ncu DRAM traffic is reported only when the record was taken on the
+    attention source that is built now (the record keys it by a source hash)."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    kid = b.run_kernel_id()
+    (tmp_path / "profiles").mkdir()
+    rec = {"workloads": {"c3_encoder_prefill": {"kernel_id": kid, "traffic_bytes_per_launch": 123},
+                         "c2_decoder_replay": {"kernel_id": "0" * 16,
+                                               "traffic_bytes_per_launch": 456}}}
+    (tmp_path / "profiles" / "attn_traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(b, "ROOT", str(tmp_path))
+    monkeypatch.setattr(b, "run_kernel_id", lambda: kid)    # the hash of the real source
+    assert b.traffic_record("c3_encoder_prefill") == 123
+    assert b.traffic_record("c2_decoder_replay") is None      # taken on another source
+    assert b.traffic_record("c4_hierarchical") is None        # never measured
