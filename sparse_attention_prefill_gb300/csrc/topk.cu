@@ -859,7 +859,7 @@ topk_kernel(Batch b, const float *__restrict__ scores, int64_t ld, int k,
 // as the long-row path).  A guess that misses falls back to the 4-pass radix
 // select over the row.
 template <int NT>
-__global__ void __launch_bounds__(NT)
+__global__ void __launch_bounds__(NT, 6)   // six CTAs per SM: 40 registers, 35 KB each
 topk_list_kernel(Batch b, const float *__restrict__ scores, int64_t ld, int k,
                  int32_t *__restrict__ idx, int32_t *__restrict__ count,
                  int32_t *__restrict__ d_err) {
