@@ -173,7 +173,8 @@ CSA2_API int csa2_tail_layout(int32_t num_req, const int32_t *extend_len,
  *         written.  A row longer than ld is cut at ld (CSA2_DERR_LD); n_vis
  *         past kv_len is cut at kv_len (CSA2_DERR_RANGE_CTX).
  * Supported: head_dim == 128, n_heads in {8, 16, 32, 64}, block in [1, 64],
- * max_blocks in [1, 4096].
+ * max_blocks in [1, 4096]; q_fp4, k_fp4, q_scale and k_scale 16-byte
+ * aligned (CSA2_ERR_UNSUPPORTED otherwise).
  * ------------------------------------------------------------------------- */
 CSA2_API int csa2_index_score(const csa2_batch *b, int32_t n_heads, int32_t head_dim,
                      const uint8_t *q_fp4, const float *q_scale,
@@ -310,7 +311,8 @@ CSA2_API int csa2_index_topk_static(const csa2_batch *b, int32_t n_heads, int32_
  *   idx      [Nq, k] int32 or NULL (k ignored)
  *   lse      [Nq, n_heads] fp32 or NULL
  * Supported: dim == 512, n_heads in {16, 32, 64}, 0 <= k <= 2048,
- * 1 <= window <= 1024.
+ * 1 <= window <= 1024; q_bf16, kv_fp8 and swa_fp8 16-byte aligned
+ * (CSA2_ERR_UNSUPPORTED otherwise).
  * ------------------------------------------------------------------------- */
 CSA2_API int csa2_sparse_swa_attn(const csa2_batch *b, int32_t n_heads, int32_t dim,
                          const void *q_bf16, const uint8_t *kv_fp8,
